@@ -1,0 +1,178 @@
+/*
+ * uno.h -- C ABI of the Uno draft+verify hot path (libuno.so, sm_103a).
+ *
+ * Two operations make up one decoding step of a diffusion-augmented LLM:
+ *
+ *   1. the gated-LoRA linear projection
+ *          y = x.W_AR^T + g_row * (alpha/rank) * (x.A^T).B^T
+ *      where draft rows (gate 1) use the AR weights plus the diffusion
+ *      adapter and verification rows (gate 0) use the AR weights only
+ *      ("Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ *      aifromscratch.in explainer, section "Two Decoupled Weight Sets":
+ *      rank-128 LoRA adapters with alpha=256, coupled through a gate);
+ *
+ *   2. the block verifier of the Psi-Spec linear sampler: rejection sampling
+ *      of a drafted block against the AR distribution that accepts the
+ *      longest valid prefix and keeps the AR output distribution exact
+ *      (same page, section "The Psi-Spec Sampler"; "Uno Uses Discrete
+ *      Diffusion to Accelerate LLMs Without Loss", cctest.ai, section
+ *      "What 'lossless' means here").
+ *
+ * A third entry point draws the drafted block itself (one candidate per
+ * position, the linear sampler's drafting half).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, except
+ *     where an argument says otherwise.  The library allocates no device or
+ *     host memory on the compute path and keeps no per-call state.  (It
+ *     caches the driver entry point used to encode TMA descriptors and the
+ *     per-device SM count and kernel attributes.)
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous and stream-ordered; the library never
+ *     synchronises.  Workspace must not be shared by calls that may overlap
+ *     on the GPU.
+ *   - Host-detectable errors (null pointers, bad sizes, misalignment, small
+ *     workspace) return a negative uno_status before anything is enqueued.
+ *     A CUDA launch error returns UNO_ERR_CUDA.  Errors the GPU detects in
+ *     the data (a draft id outside [0,V), a NaN or +inf logit) are reported
+ *     per sequence in `status` (see UNO_SEQ_*), never by trapping.
+ *   - Row-major layouts; "[a,b]" means a rows of b contiguous elements.
+ *   - Sizes are int64_t; a size of 0 where allowed is a no-op returning
+ *     UNO_OK.
+ *   - Device pointers must be 16-byte aligned.
+ */
+#ifndef UNO_H_
+#define UNO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *uno_stream_t;
+
+typedef enum {
+    UNO_OK = 0,
+    UNO_ERR_ARG = -1,         /* null pointer, negative or unsupported size */
+    UNO_ERR_ALIGN = -2,       /* pointer or row stride not 16-byte aligned  */
+    UNO_ERR_UNSUPPORTED = -3, /* dtype or shape outside what is built       */
+    UNO_ERR_WORKSPACE = -4,   /* ws_bytes smaller than the query returned   */
+    UNO_ERR_CUDA = -5         /* a CUDA runtime/driver call failed          */
+} uno_status;
+
+typedef enum {
+    UNO_F32 = 0,  /* float32 inputs and output (inputs rounded to bf16 for the
+                     tensor cores, fp32 accumulation, fp32 output)          */
+    UNO_BF16 = 1  /* bfloat16 inputs and output, fp32 accumulation         */
+} uno_dtype;
+
+/* Per-sequence (or per-row) status written by the device. */
+enum {
+    UNO_SEQ_OK = 0,
+    UNO_SEQ_BAD_DRAFT = 1, /* a draft id outside [0, V)                     */
+    UNO_SEQ_NONFINITE = 2  /* a NaN or +inf logit, or a row that is all -inf */
+};
+
+/* ---------------------------------------------------------------------------
+ * Gated-LoRA linear projection
+ *   y[m,n] = sum_k x[m,k] W[n,k] + gate[m] * (alpha/rank) * sum_j T[m,j] B[n,j]
+ *   T[m,j] = sum_k x[m,k] A[j,k]
+ * ("Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ *  aifromscratch.in, "Two Decoupled Weight Sets".)
+ *
+ *   x    [M, d_in]      activations (dtype)
+ *   W    [d_out, d_in]  theta_AR, nn.Linear layout (dtype)
+ *   A    [rank, d_in]   theta_Delta down-projection (dtype)
+ *   B    [d_out, rank]  theta_Delta up-projection (dtype)
+ *   gate [M]            uint8 per row: 1 = draft row, 0 = verification row
+ *                       (any other value is used as the multiplier itself)
+ *   y    [M, d_out]     output (dtype); must not alias any input
+ *   workspace           device scratch of at least
+ *                       uno_gated_lora_linear_workspace(...) bytes, 256-byte
+ *                       aligned; contents on entry are ignored.
+ * Arithmetic: bf16 operands on the tcgen05 tensor cores, fp32 accumulation
+ * in tensor memory.  (x.A^T) is scaled by gate*alpha/rank in fp32 and
+ * rounded to bf16 before the up-projection, which runs as extra K-blocks of
+ * the same accumulator as x.W^T.  Gate-0 rows therefore equal the plain
+ * x.W^T of the same kernel bit for bit.  Deterministic: the same inputs
+ * give the same bits on every call.
+ * Requirements: M >= 0, d_in >= 1, d_out >= 1, rank in [0, 256], d_in,
+ * d_out and rank multiples of 8; alpha finite.  rank == 0 gives x.W^T.
+ * The workspace query returns the bytes for the device current at the time
+ * of the call; use the same device for the compute call.
+ * ------------------------------------------------------------------------- */
+size_t uno_gated_lora_linear_workspace(int64_t M, int64_t d_in, int64_t d_out,
+                                       int64_t rank, int dtype);
+
+int uno_gated_lora_linear(const void *x, const void *W, const void *A,
+                          const void *B, const uint8_t *gate, int64_t M,
+                          int64_t d_in, int64_t d_out, int64_t rank,
+                          float alpha, int dtype, void *y, void *workspace,
+                          size_t ws_bytes, uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Block verifier (Psi-Spec linear sampler, verification half).
+ * ("Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ *  aifromscratch.in, "The Psi-Spec Sampler"; "Uno Uses Discrete Diffusion to
+ *  Accelerate LLMs Without Loss", cctest.ai, "What 'lossless' means here".)
+ *
+ * For each sequence b, with p_i = softmax(p_logits[b,i,:]) and
+ * q_i = softmax(q_logits[b,i,:]) (temperature 1):
+ *   accept draft i iff u_accept[b,i] < min(1, p_i(x_i) / q_i(x_i)),
+ *   n = length of the accepted prefix;
+ *   if n < K: one token from max(0, p_n - q_n) normalised (p_n if that is
+ *             all zero), drawn by the exponential race
+ *             argmax_v r(v) / (-ln u_resample[b,v]);
+ *   else if Kp == K+1: the bonus token from p_K by the same race;
+ *   out_tokens[b,0..n-1] = drafts, out_tokens[b,n] = the drawn token,
+ *   remaining entries -1; n_emitted[b] = n + (a token was drawn).
+ *
+ *   p_logits   [Bn, Kp, V] float32 AR logits, Kp == K or K+1
+ *   q_logits   [Bn, K, V]  float32 draft logits
+ *   draft      [Bn, K]     int32 drafted ids
+ *   u_accept   [Bn, K]     float32 in [0,1)
+ *   u_resample [Bn, V]     float32 in (0,1)
+ *   n_accepted [Bn], out_tokens [Bn, K+1], n_emitted [Bn], status [Bn]
+ *              int32 outputs; a sequence with status != 0 has n = 0,
+ *              n_emitted = 0 and out_tokens all -1.
+ *   workspace  at least uno_verify_block_workspace(Bn, K, Kp, V) bytes,
+ *              256-byte aligned, contents ignored on entry.
+ * Requirements: Bn >= 0, K >= 0, Kp in {K, K+1}, Kp >= 1, 1 <= V < 2^31.
+ * Logit rows need not be 16-byte aligned (any V works).
+ * ------------------------------------------------------------------------- */
+size_t uno_verify_block_workspace(int64_t Bn, int64_t K, int64_t Kp, int64_t V);
+
+int uno_verify_block(const float *p_logits, const float *q_logits,
+                     const int32_t *draft, const float *u_accept,
+                     const float *u_resample, int64_t Bn, int64_t K,
+                     int64_t Kp, int64_t V, int32_t *n_accepted,
+                     int32_t *out_tokens, int32_t *n_emitted, int32_t *status,
+                     void *workspace, size_t ws_bytes, uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Draft sampling (Psi-Spec linear sampler, drafting half: one candidate per
+ * position; "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ * aifromscratch.in, "The Psi-Spec Sampler").
+ *   tokens[r] = argmax_v softmax(logits[r,:])(v) / (-ln u[r,v])
+ * which draws v with probability softmax(logits[r,:])(v).
+ *   logits [R, V] float32, u [R, V] float32 in (0,1), tokens [R] int32,
+ *   status [R] int32 (UNO_SEQ_NONFINITE rows get token -1).
+ * Requirements: R >= 0, 1 <= V < 2^31.  No workspace.
+ * ------------------------------------------------------------------------- */
+int uno_draft_sample(const float *logits, const float *u, int64_t R, int64_t V,
+                     int32_t *tokens, int32_t *status, uno_stream_t stream);
+
+/* Human-readable text for a uno_status code (static storage). */
+const char *uno_status_string(int code);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int uno_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UNO_H_ */
