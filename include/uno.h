@@ -165,6 +165,12 @@ int uno_verify_block(const float *p_logits, const float *q_logits,
 int uno_draft_sample(const float *logits, const float *u, int64_t R, int64_t V,
                      int32_t *tokens, int32_t *status, uno_stream_t stream);
 
+/* Device error word of this library on the current device (synchronous).
+ * Bit 0 is set when a pipeline wait inside a projection kernel exceeded its
+ * 2-second limit; that kernel unwound without writing its output tile.
+ * reset != 0 clears the word.  Returns the word (>= 0) or UNO_ERR_CUDA. */
+int uno_device_error(int reset);
+
 /* Human-readable text for a uno_status code (static storage). */
 const char *uno_status_string(int code);
 

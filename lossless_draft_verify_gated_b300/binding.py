@@ -1,0 +1,174 @@
+"""ctypes binding of libuno.so with the same names as the C ABI (include/uno.h).
+
+Argument marshalling only: tensors become device pointers, missing outputs and
+workspaces are allocated with torch, the current torch stream is passed
+through.  Every step of the computation runs in libuno.so's kernels; there is
+no fallback.  If the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libuno.so")
+
+UNO_OK = 0
+UNO_ERR_ARG = -1
+UNO_ERR_ALIGN = -2
+UNO_ERR_UNSUPPORTED = -3
+UNO_ERR_WORKSPACE = -4
+UNO_ERR_CUDA = -5
+UNO_F32 = 0
+UNO_BF16 = 1
+UNO_SEQ_OK = 0
+UNO_SEQ_BAD_DRAFT = 1
+UNO_SEQ_NONFINITE = 2
+
+# Every function the header declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "uno_gated_lora_linear_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I]),
+    "uno_gated_lora_linear": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float, _I,
+                                   _P, _P, _SZ, _P]),
+    "uno_verify_block_workspace": (_SZ, [_I64, _I64, _I64, _I64]),
+    "uno_verify_block": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ,
+                              _P]),
+    "uno_draft_sample": (_I, [_P, _P, _I64, _I64, _P, _P, _P]),
+    "uno_device_error": (_I, [_I]),
+    "uno_status_string": (ctypes.c_char_p, [_I]),
+    "uno_version": (_I, []),
+}
+
+_lib = None
+
+
+class UnoError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libuno.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libuno.so not built ({LIB_PATH}); run "
+                               "`python -m lossless_draft_verify_gated_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().uno_status_string(int(code)).decode()
+
+
+def _dptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libuno takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libuno takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, rc):
+    if rc != UNO_OK:
+        raise UnoError(fn, rc)
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+_DT = {torch.float32: UNO_F32, torch.bfloat16: UNO_BF16}
+
+
+def uno_gated_lora_linear_workspace(M, d_in, d_out, rank, dtype) -> int:
+    dt = _DT[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(lib().uno_gated_lora_linear_workspace(M, d_in, d_out, rank, dt))
+
+
+def uno_gated_lora_linear(x, W, A, B, gate, alpha, *, y=None, workspace=None, stream=None):
+    """y = x.W^T + gate * (alpha/rank) * (x.A^T).B^T (see include/uno.h)."""
+    M, d_in = x.shape
+    d_out = W.shape[0]
+    rank = A.shape[0]
+    dt = _DT[x.dtype]
+    if y is None:
+        y = torch.empty((M, d_out), dtype=x.dtype, device=x.device)
+    if workspace is None:
+        workspace = _workspace(uno_gated_lora_linear_workspace(M, d_in, d_out, rank, dt), x.device)
+    rc = lib().uno_gated_lora_linear(_dptr(x), _dptr(W), _dptr(A), _dptr(B), _dptr(gate), M, d_in,
+                                     d_out, rank, float(alpha), dt, _dptr(y), _dptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    _check("uno_gated_lora_linear", rc)
+    return y
+
+
+def uno_verify_block_workspace(Bn, K, Kp, V) -> int:
+    return int(lib().uno_verify_block_workspace(Bn, K, Kp, V))
+
+
+def uno_verify_block(p_logits, q_logits, draft, u_accept, u_resample, *, out=None, workspace=None,
+                     stream=None):
+    """Returns (n_accepted [Bn], out_tokens [Bn, K+1], n_emitted [Bn], status [Bn]), int32."""
+    Bn, Kp, V = p_logits.shape
+    K = q_logits.shape[1]
+    dev = p_logits.device
+    if out is None:
+        out = (torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty((Bn, K + 1), dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev))
+    n_acc, toks, n_em, st = out
+    if workspace is None:
+        workspace = _workspace(uno_verify_block_workspace(Bn, K, Kp, V), dev)
+    rc = lib().uno_verify_block(_dptr(p_logits), _dptr(q_logits), _dptr(draft), _dptr(u_accept),
+                                _dptr(u_resample), Bn, K, Kp, V, _dptr(n_acc), _dptr(toks),
+                                _dptr(n_em), _dptr(st), _dptr(workspace), workspace.numel(),
+                                _stream(stream))
+    _check("uno_verify_block", rc)
+    return n_acc, toks, n_em, st
+
+
+def uno_draft_sample(logits, u, *, tokens=None, status=None, stream=None):
+    """tokens[r] ~ softmax(logits[r]) via the exponential race on u.  Returns (tokens, status)."""
+    V = logits.shape[-1]
+    R = logits.numel() // V if V else 0
+    shape = logits.shape[:-1]
+    if tokens is None:
+        tokens = torch.empty(shape, dtype=torch.int32, device=logits.device)
+    if status is None:
+        status = torch.empty(shape, dtype=torch.int32, device=logits.device)
+    rc = lib().uno_draft_sample(_dptr(logits), _dptr(u), R, V, _dptr(tokens), _dptr(status),
+                                _stream(stream))
+    _check("uno_draft_sample", rc)
+    return tokens, status
+
+
+def uno_device_error(reset: bool = False) -> int:
+    return int(lib().uno_device_error(1 if reset else 0))
+
+
+def uno_version() -> int:
+    return int(lib().uno_version())

@@ -1,0 +1,138 @@
+// api.cu -- the extern "C" boundary of libuno.so (declared in include/uno.h):
+// argument validation, workspace queries and dispatch to the kernels.
+// Everything here runs on the host and touches no device memory.
+#include <cstdint>
+#include <mutex>
+
+#include "uno_internal.h"
+
+namespace uno {
+
+int read_device_error(int reset);  // gemm.cu
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 148;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+bool lora_shape_ok(int64_t M, int64_t d_in, int64_t d_out, int64_t rank, int dtype) {
+  if (M < 0 || d_in < 1 || d_out < 1 || rank < 0 || rank > 256) return false;
+  if (d_in % 8 || d_out % 8 || rank % 8) return false;
+  if (dtype != UNO_F32 && dtype != UNO_BF16) return false;
+  if (M > (int64_t(1) << 31) - 1 || d_in > (int64_t(1) << 31) - 1 || d_out > (int64_t(1) << 31) - 1)
+    return false;
+  return true;
+}
+
+bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V) {
+  if (Bn < 0 || K < 0 || K > 256 || V < 1 || V >= (int64_t(1) << 31)) return false;
+  if (Kp != K && Kp != K + 1) return false;
+  if (Kp < 1) return false;
+  if (Bn > (int64_t(1) << 24)) return false;
+  return true;
+}
+
+}  // namespace
+}  // namespace uno
+
+using namespace uno;
+
+extern "C" {
+
+int uno_version(void) { return 100; }
+
+const char* uno_status_string(int code) {
+  switch (code) {
+    case UNO_OK: return "ok";
+    case UNO_ERR_ARG: return "invalid argument (null pointer, bad size or unsupported shape)";
+    case UNO_ERR_ALIGN: return "pointer or row stride not 16-byte aligned";
+    case UNO_ERR_UNSUPPORTED: return "unsupported dtype or shape";
+    case UNO_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case UNO_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+size_t uno_gated_lora_linear_workspace(int64_t M, int64_t d_in, int64_t d_out, int64_t rank,
+                                       int dtype) {
+  if (!lora_shape_ok(M, d_in, d_out, rank, dtype)) return 0;
+  return lora_workspace_bytes(M, d_in, d_out, rank, dtype, sm_count());
+}
+
+int uno_gated_lora_linear(const void* x, const void* W, const void* A, const void* B,
+                          const uint8_t* gate, int64_t M, int64_t d_in, int64_t d_out,
+                          int64_t rank, float alpha, int dtype, void* y, void* workspace,
+                          size_t ws_bytes, uno_stream_t stream) {
+  if (dtype != UNO_F32 && dtype != UNO_BF16) return UNO_ERR_UNSUPPORTED;
+  if (!lora_shape_ok(M, d_in, d_out, rank, dtype)) return UNO_ERR_ARG;
+  if (!(alpha == alpha) || alpha == INFINITY || alpha == -INFINITY) return UNO_ERR_ARG;
+  if (M == 0) return UNO_OK;
+  if (!x || !W || !gate || !y || !workspace) return UNO_ERR_ARG;
+  if (rank > 0 && (!A || !B)) return UNO_ERR_ARG;
+  if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (rank > 0 && (!aligned16(A) || !aligned16(B))))
+    return UNO_ERR_ALIGN;
+  if (!aligned256(workspace)) return UNO_ERR_WORKSPACE;
+  return launch_gated_lora_linear(x, W, A, B, gate, M, d_in, d_out, rank, alpha, dtype, y,
+                                  workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t uno_verify_block_workspace(int64_t Bn, int64_t K, int64_t Kp, int64_t V) {
+  if (!verify_shape_ok(Bn, K, Kp, V)) return 0;
+  return plan_verify(Bn, K, Kp, V, sm_count()).bytes;
+}
+
+int uno_verify_block(const float* p_logits, const float* q_logits, const int32_t* draft,
+                     const float* u_accept, const float* u_resample, int64_t Bn, int64_t K,
+                     int64_t Kp, int64_t V, int32_t* n_accepted, int32_t* out_tokens,
+                     int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
+                     uno_stream_t stream) {
+  if (!verify_shape_ok(Bn, K, Kp, V)) return UNO_ERR_ARG;
+  if (Bn == 0) return UNO_OK;
+  if (!p_logits || !u_resample || !n_accepted || !out_tokens || !n_emitted || !status || !workspace)
+    return UNO_ERR_ARG;
+  if (K > 0 && (!q_logits || !draft || !u_accept)) return UNO_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits) |
+       reinterpret_cast<uintptr_t>(u_resample) | reinterpret_cast<uintptr_t>(u_accept)) & 3u)
+    return UNO_ERR_ALIGN;
+  if (!aligned256(workspace)) return UNO_ERR_WORKSPACE;
+  const VerifyPlan pl = plan_verify(Bn, K, Kp, V, sm_count());
+  if (ws_bytes < pl.bytes) return UNO_ERR_WORKSPACE;
+  const cudaError_t e = launch_verify(p_logits, q_logits, draft, u_accept, u_resample, Bn, K, Kp, V,
+                                      n_accepted, out_tokens, n_emitted, status, workspace, pl,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
+}
+
+int uno_draft_sample(const float* logits, const float* u, int64_t R, int64_t V, int32_t* tokens,
+                     int32_t* status, uno_stream_t stream) {
+  if (R < 0 || V < 1 || V >= (int64_t(1) << 31) || R >= (int64_t(1) << 31)) return UNO_ERR_ARG;
+  if (R == 0) return UNO_OK;
+  if (!logits || !u || !tokens || !status) return UNO_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(u)) & 3u)
+    return UNO_ERR_ALIGN;
+  const cudaError_t e =
+      launch_draft_sample(logits, u, R, V, tokens, status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
+}
+
+int uno_device_error(int reset) { return read_device_error(reset); }
+
+}  // extern "C"

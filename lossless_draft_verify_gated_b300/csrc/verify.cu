@@ -1,0 +1,410 @@
+// verify.cu -- block verifier and draft sampler of the Psi-Spec linear sampler.
+//
+// "Unlocking Lossless Speedups in LLMs via Discrete Diffusion"
+// (aifromscratch.in), section "The Psi-Spec Sampler": a block drafted in
+// parallel is checked against the AR model by speculative-decoding-style
+// rejection sampling that keeps the longest valid prefix and preserves the AR
+// output distribution exactly; the linear sampler draws one candidate per
+// position.  "Uno Uses Discrete Diffusion to Accelerate LLMs Without Loss"
+// (cctest.ai), section "What 'lossless' means here": the AR model rejects or
+// adjusts candidates.
+//
+// The verifier is bound by HBM: every AR and draft logit is read once (8 bytes
+// per (position, vocab entry)).  Two launches:
+//   stats  -- one CTA per (row, vocab chunk); 128-bit streaming loads, an
+//             online (max, sum exp) per thread, warp-shuffle merge, one
+//             partial per CTA.  Rows of all sequences are spread over the grid,
+//             and short rows are split so the grid fills the 148 SMs.
+//   finish -- one CTA per (sequence, vocab chunk); every CTA of a sequence
+//             merges the partials of that sequence (identically), takes the
+//             accept decisions and the prefix length n, then races its chunk
+//             of the residual row (or the bonus row); the last CTA to arrive
+//             (atomic counter, no waiting) merges the chunk winners and writes
+//             the outputs.
+// Nothing spins, nothing traps: bad data sets a per-sequence status.
+#include <algorithm>
+#include <cfloat>
+#include <cmath>
+
+#include "uno_internal.h"
+
+namespace uno {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 4;
+
+struct MS {
+  float m, s;  // running max and sum of exp(x - m)
+};
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return {m, a.s + b.s};
+  return {m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
+}
+
+// Fold four logits into a running (max, sum).  NaN poisons s; +inf makes
+// s NaN through inf - inf; -inf entries contribute exactly 0.
+__device__ __forceinline__ void ms_add4(MS& a, float x0, float x1, float x2, float x3) {
+  const float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  if (mx > a.m) {
+    a.s *= __expf(a.m - mx);
+    a.m = mx;
+  }
+  if (a.m != -INFINITY) {
+    a.s += __expf(x0 - a.m) + __expf(x1 - a.m) + __expf(x2 - a.m) + __expf(x3 - a.m);
+  } else if (isnan(x0) || isnan(x1) || isnan(x2) || isnan(x3)) {
+    a.s = NAN;
+  }
+}
+
+__device__ __forceinline__ void ms_add1(MS& a, float x) {
+  ms_add4(a, x, -INFINITY, -INFINITY, -INFINITY);
+}
+
+__device__ __forceinline__ MS warp_merge(MS a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS b{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+    a = ms_merge(a, b);
+  }
+  return a;
+}
+
+// Row j of sequence b: j < Kp is AR row j, else draft row j - Kp.
+__device__ __forceinline__ const float* row_ptr(const float* p, const float* q, int64_t b,
+                                                int64_t j, int64_t K, int64_t Kp, int64_t V) {
+  return j < Kp ? p + (b * Kp + j) * V : q + (b * K + (j - Kp)) * V;
+}
+
+__global__ void __launch_bounds__(kThreads)
+verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int64_t K,
+                    int64_t Kp, int64_t V, int splits, int64_t chunk, float2* __restrict__ part,
+                    int* __restrict__ counter) {
+  const int64_t unit = blockIdx.x;
+  const int64_t row = unit / splits;
+  const int split = int(unit - row * splits);
+  const int64_t per_seq = Kp + K;
+  const int64_t b = row / per_seq;
+  const int64_t j = row - b * per_seq;
+  if (j == 0 && split == 0 && threadIdx.x == 0) counter[b] = 0;  // finish kernel's arrival count
+
+  const float* r = row_ptr(p, q, b, j, K, Kp, V);
+  const int64_t v0 = int64_t(split) * chunk;
+  const int64_t v1 = min(V, v0 + chunk);
+  // 16-byte aligned body [va, vb), scalar head [v0, va) and tail [vb, v1).
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(r + v0);
+  const int64_t head_raw = int64_t(((16 - (addr & 15)) & 15) >> 2);
+  const int64_t head = head_raw < v1 - v0 ? head_raw : v1 - v0;
+  const int64_t va = v0 + head;
+  const int64_t nvec = (v1 - va) >> 2;
+  const int64_t vb = va + nvec * 4;
+
+  MS acc{-INFINITY, 0.f};
+  const int tid = threadIdx.x;
+  if (tid < va - v0) ms_add1(acc, r[v0 + tid]);
+  if (tid < v1 - vb) ms_add1(acc, r[vb + tid]);
+  const float4* vp = reinterpret_cast<const float4*>(r + va);
+  for (int64_t i = tid; i < nvec; i += int64_t(kThreads) * kUnroll) {
+    float4 t[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t idx = i + int64_t(u) * kThreads;
+      t[u] = idx < nvec ? __ldcs(vp + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) ms_add4(acc, t[u].x, t[u].y, t[u].z, t[u].w);
+  }
+
+  acc = warp_merge(acc);
+  __shared__ MS red[kWarps];
+  if ((tid & 31) == 0) red[tid >> 5] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    MS t = red[0];
+    for (int w = 1; w < kWarps; ++w) t = ms_merge(t, red[w]);
+    part[unit] = make_float2(t.m, t.s);
+  }
+}
+
+struct Cand {
+  float s;  // race score
+  int v;    // vocab id, -1 = none
+};
+
+__device__ __forceinline__ Cand cand_best(Cand a, Cand b) {
+  if (b.s > a.s || (b.s == a.s && b.v >= 0 && (a.v < 0 || b.v < a.v))) return b;
+  return a;
+}
+
+__device__ __forceinline__ Cand warp_best(Cand a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand b{__shfl_xor_sync(0xffffffffu, a.s, o), __shfl_xor_sync(0xffffffffu, a.v, o)};
+    a = cand_best(a, b);
+  }
+  return a;
+}
+
+struct RacePart {
+  float sr;  // best residual score in the chunk (0 if no positive residual)
+  int vr;
+  float sp;  // best score of the AR row itself (fallback and bonus race)
+  int vp;
+};
+
+constexpr int kMaxRows = 2 * 256 + 1;  // Kp + K rows of one sequence held in smem
+
+__global__ void __launch_bounds__(kThreads)
+verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                     const int32_t* __restrict__ draft, const float* __restrict__ u_acc,
+                     const float* __restrict__ u_res, int64_t K, int64_t Kp, int64_t V,
+                     int splits, int race_splits, int64_t race_chunk,
+                     const float2* __restrict__ part, RacePart* __restrict__ rpart,
+                     int* __restrict__ counter, int32_t* __restrict__ n_acc,
+                     int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_emit,
+                     int32_t* __restrict__ status) {
+  __shared__ float s_m[kMaxRows];    // row max
+  __shared__ float s_lz[kMaxRows];   // row max + ln(sum)
+  __shared__ float s_iz[kMaxRows];   // 1 / sum
+  __shared__ int s_bad;
+  __shared__ int s_n;
+  __shared__ int s_last;
+  __shared__ Cand s_cr[kWarps], s_cp[kWarps];
+
+  const int tid = threadIdx.x;
+  const int64_t b = blockIdx.x / race_splits;
+  const int split = int(blockIdx.x - b * race_splits);
+  const int64_t per_seq = Kp + K;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  // 1. Row normalisers of this sequence from the statistics partials.
+  for (int64_t j = tid; j < per_seq; j += kThreads) {
+    const float2* pp = part + (b * per_seq + j) * splits;
+    MS t{-INFINITY, 0.f};
+    for (int s = 0; s < splits; ++s) {
+      const float2 v = pp[s];
+      t = ms_merge(t, MS{v.x, v.y});
+    }
+    const bool bad = isnan(t.s) || !(t.m > -INFINITY) || !(t.m < INFINITY) || !(t.s > 0.f);
+    if (bad) atomicOr(&s_bad, 2);
+    s_m[j] = t.m;
+    s_lz[j] = t.m + logf(t.s);
+    s_iz[j] = 1.0f / t.s;
+  }
+  // 2. Draft ids and acceptance flags.
+  for (int64_t i = tid; i < K; i += kThreads) {
+    const int32_t x = draft[b * K + i];
+    if (x < 0 || x >= V) atomicOr(&s_bad, 1);
+  }
+  __syncthreads();
+  const int bad = s_bad;
+  int32_t* out = out_tokens + b * (K + 1);
+  if (bad) {
+    if (split == 0) {
+      for (int64_t i = tid; i <= K; i += kThreads) out[i] = -1;
+      if (tid == 0) {
+        n_acc[b] = 0;
+        n_emit[b] = 0;
+        status[b] = (bad & 1) ? UNO_SEQ_BAD_DRAFT : UNO_SEQ_NONFINITE;
+      }
+    }
+    return;
+  }
+  // Accept x_i iff u_i < min(1, p_i(x_i)/q_i(x_i)), the ratio taken in the
+  // log domain so that neither probability underflows.
+  if (tid == 0) s_n = int(K);
+  __syncthreads();
+  for (int64_t i = tid; i < K; i += kThreads) {
+    const int32_t x = draft[b * K + i];
+    const float lq = q[(b * K + i) * V + x];
+    bool accept;
+    if (lq == -INFINITY) {
+      accept = true;  // q_i(x) = 0: ratio +inf
+    } else {
+      const float lp = p[(b * Kp + i) * V + x];
+      const float lr = (lp - s_lz[i]) - (lq - s_lz[Kp + i]);
+      const float thr = fminf(1.0f, expf(lr));
+      accept = u_acc[b * K + i] < thr;
+    }
+    if (!accept) atomicMin(&s_n, int(i));
+  }
+  __syncthreads();
+  const int n = s_n;
+
+  const bool residual = n < K;
+  const bool bonus = !residual && Kp == K + 1;
+  if (!residual && !bonus) {
+    if (split == 0) {
+      for (int64_t i = tid; i <= K; i += kThreads) out[i] = i < K ? draft[b * K + i] : -1;
+      if (tid == 0) {
+        n_acc[b] = n;
+        n_emit[b] = n;
+        status[b] = UNO_SEQ_OK;
+      }
+    }
+    return;
+  }
+
+  // 3. Exponential race over this CTA's vocab chunk:
+  //    residual: argmax_v max(0, p_n(v) - q_n(v)) / (-ln u_v), falling back
+  //    to p_n if no entry is positive; bonus: argmax_v p_K(v) / (-ln u_v).
+  const int64_t prow = residual ? n : K;
+  const float* pr = p + (b * Kp + prow) * V;
+  const float* qr = q + (b * K + n) * V;  // only read when residual
+  const float mp = s_m[prow], izp = s_iz[prow];
+  const float mq = residual ? s_m[Kp + n] : 0.f, izq = residual ? s_iz[Kp + n] : 0.f;
+  const float* ub = u_res + b * V;
+  const int64_t v0 = int64_t(split) * race_chunk;
+  const int64_t v1 = min(V, v0 + race_chunk);
+  Cand cr{0.f, -1}, cp{-1.f, -1};
+  for (int64_t v = v0 + tid; v < v1; v += kThreads) {
+    const float e = -logf(ub[v]);
+    const float pv = expf(pr[v] - mp) * izp;
+    cp = cand_best(cp, Cand{pv / e, int(v)});
+    if (residual) {
+      const float rv = pv - expf(qr[v] - mq) * izq;
+      if (rv > 0.f) cr = cand_best(cr, Cand{rv / e, int(v)});
+    }
+  }
+  cr = warp_best(cr);
+  cp = warp_best(cp);
+  if ((tid & 31) == 0) {
+    s_cr[tid >> 5] = cr;
+    s_cp[tid >> 5] = cp;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    cr = s_cr[0];
+    cp = s_cp[0];
+    for (int w = 1; w < kWarps; ++w) {
+      cr = cand_best(cr, s_cr[w]);
+      cp = cand_best(cp, s_cp[w]);
+    }
+    int last = 1;
+    if (race_splits > 1) {
+      rpart[b * race_splits + split] = RacePart{cr.s, cr.v, cp.s, cp.v};
+      __threadfence();
+      last = atomicAdd(&counter[b], 1) == race_splits - 1;
+      if (last) {
+        __threadfence();
+        cr = Cand{0.f, -1};
+        cp = Cand{-1.f, -1};
+        for (int s = 0; s < race_splits; ++s) {
+          const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
+          cr = cand_best(cr, Cand{__int_as_float(t.x), t.y});
+          cp = cand_best(cp, Cand{__int_as_float(t.z), t.w});
+        }
+        counter[b] = 0;
+      }
+    }
+    s_last = last;
+    if (last) {
+      const int tok = (residual && cr.v >= 0) ? cr.v : cp.v;
+      n_acc[b] = n;
+      n_emit[b] = n + 1;
+      status[b] = UNO_SEQ_OK;
+      s_n = tok;
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  const int tok = s_n;
+  for (int64_t i = tid; i <= K; i += kThreads)
+    out[i] = i < n ? draft[b * K + i] : (i == n ? tok : -1);
+}
+
+// One CTA per row: Gumbel-max form of the race, argmax_v l_v - ln(-ln u_v),
+// which equals argmax_v softmax(l)(v) / (-ln u_v) (the normaliser cancels).
+__global__ void __launch_bounds__(kThreads)
+draft_sample_kernel(const float* __restrict__ logits, const float* __restrict__ u, int64_t V,
+                    int32_t* __restrict__ tokens, int32_t* __restrict__ status) {
+  __shared__ Cand s_c[kWarps];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  const int64_t r = blockIdx.x;
+  const float* lr = logits + r * V;
+  const float* ur = u + r * V;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  Cand c{-INFINITY, -1};
+  bool bad = false;
+  for (int64_t v = tid; v < V; v += kThreads) {
+    const float l = __ldcs(lr + v);
+    bad |= isnan(l) || l == INFINITY;
+    if (l > -INFINITY) c = cand_best(c, Cand{l - logf(-logf(__ldcs(ur + v))), int(v)});
+  }
+  if (bad) atomicOr(&s_bad, 1);
+  c = warp_best(c);
+  if ((tid & 31) == 0) s_c[tid >> 5] = c;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kWarps; ++w) c = cand_best(c, s_c[w]);
+    if (s_bad || c.v < 0) {
+      tokens[r] = -1;
+      status[r] = UNO_SEQ_NONFINITE;
+    } else {
+      tokens[r] = c.v;
+      status[r] = UNO_SEQ_OK;
+    }
+  }
+}
+
+}  // namespace
+
+VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
+  VerifyPlan pl{};
+  pl.rows = Bn * (Kp + K);
+  // Statistics pass: about 8 CTAs of 256 threads per SM in flight; split
+  // rows only while each chunk keeps at least 2048 logits.
+  const int64_t target = int64_t(sms) * 8;
+  int64_t s = pl.rows > 0 ? (target + pl.rows - 1) / pl.rows : 1;
+  s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 2047) / 2048));
+  int64_t chunk = (V + s - 1) / s;
+  chunk = (chunk + 3) & ~int64_t(3);
+  pl.chunk = chunk;
+  pl.splits = int((V + chunk - 1) / chunk);
+  // Race pass: about 4 CTAs per SM, chunks of at least 4096 entries.
+  const int64_t rt = int64_t(sms) * 4;
+  int64_t s2 = Bn > 0 ? (rt + Bn - 1) / Bn : 1;
+  s2 = std::max<int64_t>(1, std::min<int64_t>(s2, (V + 4095) / 4096));
+  pl.race_chunk = (V + s2 - 1) / s2;
+  pl.race_splits = int((V + pl.race_chunk - 1) / pl.race_chunk);
+  pl.off_stats = 0;
+  pl.off_race = align_up(pl.off_stats + size_t(pl.rows) * pl.splits * sizeof(float2), 256);
+  pl.off_count = align_up(pl.off_race + size_t(Bn) * pl.race_splits * sizeof(RacePart), 256);
+  pl.bytes = align_up(pl.off_count + size_t(Bn) * sizeof(int), 256);
+  return pl;
+}
+
+cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
+                          const float* u_acc, const float* u_res, int64_t Bn, int64_t K,
+                          int64_t Kp, int64_t V, int32_t* n_acc, int32_t* out_tokens,
+                          int32_t* n_emit, int32_t* status, void* ws, const VerifyPlan& pl,
+                          cudaStream_t st) {
+  char* w = static_cast<char*>(ws);
+  float2* part = reinterpret_cast<float2*>(w + pl.off_stats);
+  RacePart* rpart = reinterpret_cast<RacePart*>(w + pl.off_race);
+  int* counter = reinterpret_cast<int*>(w + pl.off_count);
+  const int64_t g1 = pl.rows * pl.splits;
+  verify_stats_kernel<<<dim3(unsigned(g1)), kThreads, 0, st>>>(p, q, K, Kp, V, pl.splits,
+                                                                pl.chunk, part, counter);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t g2 = Bn * pl.race_splits;
+  verify_finish_kernel<<<dim3(unsigned(g2)), kThreads, 0, st>>>(
+      p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, part,
+      rpart, counter, n_acc, out_tokens, n_emit, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_sample(const float* logits, const float* u, int64_t R, int64_t V,
+                                int32_t* tokens, int32_t* status, cudaStream_t st) {
+  draft_sample_kernel<<<dim3(unsigned(R)), kThreads, 0, st>>>(logits, u, V, tokens, status);
+  return cudaGetLastError();
+}
+
+}  // namespace uno

@@ -1,0 +1,113 @@
+"""GPU parity of the gated-LoRA projection against the fp64 oracle:
+max |y_gpu - y_ref| <= 2e-2 * rms(y_ref) with bf16 operands and fp32
+accumulation, plus the exact structural properties of the gate.
+("Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+aifromscratch.in, section "Two Decoupled Weight Sets".)"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import GEMM_TOL, gemm_err, require_gpu
+from lossless_draft_verify_gated_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _gpu_run(pr, **kw):
+    from lossless_draft_verify_gated_b300 import uno_gated_lora_linear
+    d = "cuda"
+    y = uno_gated_lora_linear(pr.x.to(d), pr.W.to(d), pr.A.to(d), pr.B.to(d), pr.gate.to(d),
+                              pr.alpha, **kw)
+    torch.cuda.synchronize()
+    return y
+
+
+def _ref(pr, rows=None):
+    x, g = (pr.x, pr.gate) if rows is None else (pr.x[rows], pr.gate[rows])
+    return oracle.gated_lora_linear(x, pr.W, pr.A, pr.B, g, pr.alpha)
+
+
+@pytest.mark.parametrize("M,d_in,d_out,r,alpha,dtype,block", [
+    (16, 256, 256, 16, 32.0, torch.float32, 4),     # tiny smoke configuration (fp32 in/out)
+    (16, 256, 256, 16, 32.0, torch.bfloat16, 4),
+    (13, 200, 136, 24, 48.0, torch.bfloat16, 4),    # ragged M, K tail, N tail, rank not /64
+    (32, 4096, 1024, 128, 256.0, torch.bfloat16, 16),  # k/v projection shape at decode M
+    (100, 512, 384, 128, 256.0, torch.bfloat16, 16),   # swap path, 128-wide token tile
+    (256, 1024, 520, 64, 128.0, torch.bfloat16, 16),   # largest swap tile
+    (300, 512, 1000, 128, 256.0, torch.bfloat16, 16),  # non-swap path, ragged M and N
+    (40, 64, 64, 8, 16.0, torch.bfloat16, 16),         # single K-block
+])
+def test_lora_parity(M, d_in, d_out, r, alpha, dtype, block):
+    pr = inputs.lora_problem(M, d_in, d_out, r, alpha, dtype=dtype, block=block,
+                             name=f"t.{M}.{d_in}.{d_out}.{r}")
+    y = _gpu_run(pr)
+    assert y.dtype == dtype and y.shape == (M, d_out)
+    ref = _ref(pr)
+    assert gemm_err(y, ref) <= GEMM_TOL
+    # the adapter term is really there: the error against the base GEMM alone is large
+    base = oracle.gated_lora_linear(pr.x, pr.W, pr.A, pr.B, torch.zeros_like(pr.gate), pr.alpha)
+    if pr.gate.any():
+        assert gemm_err(y, base) > 5 * gemm_err(y, ref)
+
+
+@pytest.mark.parametrize("name,d_in,d_out", inputs.LLAMA3_8B_PROJECTIONS)
+def test_llama3_layer_decode_parity(name, d_in, d_out):
+    """Each projection of the Llama-3-8B-shaped layer at batch 1 x block 16 (M = 32)."""
+    pr = inputs.lora_problem(32, d_in, d_out, 128, 256.0, block=16, name=f"llama3.{name}",
+                             x_name=f"llama3.{inputs.LLAMA3_8B_INPUT_OF[name]}")
+    y = _gpu_run(pr)
+    assert gemm_err(y, _ref(pr)) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("M", [2048])
+@pytest.mark.parametrize("name,d_in,d_out", [inputs.LLAMA3_8B_PROJECTIONS[0],
+                                             inputs.LLAMA3_8B_PROJECTIONS[4],
+                                             inputs.LLAMA3_8B_PROJECTIONS[6]])
+def test_llama3_layer_large_m_sampled(M, name, d_in, d_out):
+    """Batch 64 x block 16 (M = 2048): 64 seeded rows (half gate 0, half gate 1)
+    are checked against the oracle over every column."""
+    pr = inputs.lora_problem(M, d_in, d_out, 128, 256.0, block=16, name=f"llama3.{name}",
+                             x_name=f"llama3.{inputs.LLAMA3_8B_INPUT_OF[name]}")
+    y = _gpu_run(pr)
+    g = inputs.generator(f"rows.{name}.{M}")
+    rows = torch.randperm(M, generator=g)[:64]
+    ref = _ref(pr, rows)
+    assert gemm_err(y[rows.cuda()], ref) <= GEMM_TOL
+    assert pr.gate[rows].sum() > 0 and (pr.gate[rows] == 0).sum() > 0
+
+
+def test_gate_zero_rows_bit_equal_all_gates_zero():
+    pr = inputs.lora_problem(32, 4096, 4096, 128, 256.0, name="gz")
+    y = _gpu_run(pr)
+    pr0 = inputs.LoraProblem(pr.x, pr.W, pr.A, pr.B, torch.zeros_like(pr.gate), pr.alpha)
+    y0 = _gpu_run(pr0)
+    z = (pr.gate == 0).cuda()
+    assert torch.equal(y[z].view(torch.int16), y0[z].view(torch.int16))
+    assert not torch.equal(y[~z], y0[~z])
+
+
+def test_rank_zero_and_alpha_zero():
+    pr = inputs.lora_problem(24, 512, 256, 32, 64.0, name="r0")
+    base = oracle.gated_lora_linear(pr.x, pr.W, pr.A, pr.B, torch.zeros_like(pr.gate), 0.0)
+    pr_r0 = inputs.LoraProblem(pr.x, pr.W, pr.A[:0], pr.B[:, :0].contiguous(), pr.gate, pr.alpha)
+    assert gemm_err(_gpu_run(pr_r0), base) <= GEMM_TOL
+    pr_a0 = inputs.LoraProblem(pr.x, pr.W, pr.A, pr.B, pr.gate, 0.0)
+    assert gemm_err(_gpu_run(pr_a0), base) <= GEMM_TOL
+
+
+def test_deterministic():
+    pr = inputs.lora_problem(32, 4096, 14336, 128, 256.0, name="det")
+    a = _gpu_run(pr)
+    b = _gpu_run(pr)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_no_device_error_flag():
+    from lossless_draft_verify_gated_b300 import uno_device_error
+    assert uno_device_error() == 0
