@@ -153,6 +153,33 @@ int uno_verify_block(const float *p_logits, const float *q_logits,
                      void *workspace, size_t ws_bytes, uno_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Block verifier that allocates nothing (the paper has no counterpart: this is
+ * a library convenience).  For callers that cannot provide device scratch --
+ * e.g. an op embedded in another runtime that receives only its input and
+ * output buffers, or a serving path whose memory belongs to a pool it may not
+ * grow or where cudaMalloc is forbidden.  Same arguments, semantics and
+ * outputs as uno_verify_block, minus the workspace: the scratch is a fixed
+ * array of uno_verify_block_no_alloc_max_scratch() bytes (8 MiB) inside the
+ * library, present on every GPU that loads it until the process exits.
+ *   - Returns UNO_ERR_WORKSPACE, without launching anything, when the call
+ *     needs more scratch than the array holds (uno_verify_block_workspace()
+ *     of the same sizes is what it needs).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array: calls that can overlap on the GPU (other
+ *     streams, other threads) race on it; the caller must serialise them.
+ *   - Calls no allocating routine (no cudaMalloc/cudaFree).
+ * ------------------------------------------------------------------------- */
+size_t uno_verify_block_no_alloc_max_scratch(void);
+
+int uno_verify_block_no_alloc(const float *p_logits, const float *q_logits,
+                              const int32_t *draft, const float *u_accept,
+                              const float *u_resample, int64_t Bn, int64_t K,
+                              int64_t Kp, int64_t V, int32_t *n_accepted,
+                              int32_t *out_tokens, int32_t *n_emitted,
+                              int32_t *status, uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Draft sampling (Psi-Spec linear sampler, drafting half: one candidate per
  * position; "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
  * aifromscratch.in, "The Psi-Spec Sampler").

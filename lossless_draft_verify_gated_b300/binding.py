@@ -40,6 +40,9 @@ SIGNATURES = {
     "uno_verify_block": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ,
                               _P]),
     "uno_draft_sample": (_I, [_P, _P, _I64, _I64, _P, _P, _P]),
+    "uno_verify_block_no_alloc_max_scratch": (_SZ, []),
+    "uno_verify_block_no_alloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
+                                       _P]),
     "uno_device_error": (_I, [_I]),
     "uno_status_string": (ctypes.c_char_p, [_I]),
     "uno_version": (_I, []),
