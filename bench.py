@@ -159,7 +159,7 @@ class Step:
                                 dtype=torch.uint8, device=device) for _, p in self.layer]
         vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=device)
         self.p, self.q, self.ua, self.ur = vp.p_logits, vp.q_logits, vp.u_accept, vp.u_resample
-        # drafts: the linear sampler's drafting half, one candidate per position from q
+        # drafts: the linear sampler's drafting half, a single token drawn from q at each position
         self.draft, st = binding.uno_draft_sample(self.q, vp.u_draft)
         assert int(st.abs().sum()) == 0
         del vp

@@ -9,16 +9,18 @@
  *      adapter and verification rows (gate 0) use the AR weights only
  *      ("Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
  *      aifromscratch.in explainer, section "Two Decoupled Weight Sets":
- *      rank-128 LoRA adapters with alpha=256, coupled through a gate);
+ *      the adapters have rank 128 and alpha 256 and are coupled through a
+ *      gate);
  *
  *   2. the block verifier of the Psi-Spec linear sampler: rejection sampling
  *      of a drafted block against the AR distribution that accepts the
- *      longest valid prefix and keeps the AR output distribution exact
+ *      drafts up to the first rejection and leaves the emitted tokens
+ *      distributed exactly as the AR model's
  *      (same page, section "The Psi-Spec Sampler"; "Uno Uses Discrete
  *      Diffusion to Accelerate LLMs Without Loss", cctest.ai, section
  *      "What 'lossless' means here").
  *
- * A third entry point draws the drafted block itself (one candidate per
+ * A third entry point draws the drafted block itself (a single token at each
  * position, the linear sampler's drafting half).
  *
  * Conventions shared by every entry point
@@ -180,8 +182,8 @@ int uno_verify_block_no_alloc(const float *p_logits, const float *q_logits,
                               int32_t *status, uno_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Draft sampling (Psi-Spec linear sampler, drafting half: one candidate per
- * position; "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ * Draft sampling (Psi-Spec linear sampler, drafting half: a single token at
+ * each position; "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
  * aifromscratch.in, "The Psi-Spec Sampler").
  *   tokens[r] = argmax_v softmax(logits[r,:])(v) / (-ln u[r,v])
  * which draws v with probability softmax(logits[r,:])(v).

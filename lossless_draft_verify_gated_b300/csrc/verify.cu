@@ -2,10 +2,10 @@
 //
 // "Unlocking Lossless Speedups in LLMs via Discrete Diffusion"
 // (aifromscratch.in), section "The Psi-Spec Sampler": a block drafted in
-// parallel is checked against the AR model by speculative-decoding-style
-// rejection sampling that keeps the longest valid prefix and preserves the AR
-// output distribution exactly; the linear sampler draws one candidate per
-// position.  "Uno Uses Discrete Diffusion to Accelerate LLMs Without Loss"
+// parallel is checked against the AR model by rejection sampling (as in
+// speculative decoding): drafts are kept up to the first rejection and the
+// emitted tokens follow the AR model's distribution; the linear sampler draws
+// a single token at each position.  "Uno Uses Discrete Diffusion to Accelerate LLMs Without Loss"
 // (cctest.ai), section "What 'lossless' means here": the AR model rejects or
 // adjusts candidates.
 //

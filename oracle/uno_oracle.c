@@ -23,14 +23,15 @@
  *       verification rows use theta_AR only.  Pinned by a hand-worked golden
  *       example, by numpy matmul for gate-0 rows, by the merged-weight form
  *       x.(W + (alpha/r) B A)^T for gate-1 rows, and by alpha=0 / B=0.
- *   oracle_verify_block_f64 -- [Explainer] "The Psi-Spec Sampler" (reject
- *       sampling against the AR model, longest valid prefix, AR distribution
- *       kept exactly); [Article] "What 'lossless' means here".  Pinned by
+ *   oracle_verify_block_f64 -- [Explainer] "The Psi-Spec Sampler" (the drafts
+ *       are rejection-sampled against the AR model; the accepted run ends at
+ *       the first rejection; emitted tokens follow the AR model's
+ *       distribution); [Article] "What 'lossless' means here".  Pinned by
  *       q==p => all accepted, disjoint supports => none accepted, the closed
  *       form E[n] = sum_k prod_{i<k} alpha_i, the acceptance threshold placed
  *       at min(1, p/q), and chi-square tests of the emitted tokens against p.
  *   oracle_draft_sample_f64 -- [Explainer] "The Psi-Spec Sampler" (the linear
- *       sampler draws one candidate per position).  Pinned by chi-square
+ *       sampler draws a single token at each position).  Pinned by chi-square
  *       against softmax(logits).
  *
  * Readings where the pages are silent (each restated in the design doc):
@@ -64,8 +65,9 @@
 /* Gated-LoRA linear projection.                                            */
 /*   y[m,n] = sum_k x[m,k] W[n,k]                                           */
 /*          + g[m] * (alpha/rank) * sum_j (sum_k x[m,k] A[j,k]) B[n,j]       */
-/* [Explainer] "Two Decoupled Weight Sets": the draft pathway uses both     */
-/* weight sets (gate 1), the verification pathway only theta_AR (gate 0).   */
+/* [Explainer] "Two Decoupled Weight Sets": rows of the draft pathway get   */
+/* theta_AR plus the adapter (gate 1); verification rows get theta_AR alone  */
+/* (gate 0).                                                                 */
 /* All inputs are already fp64 (bf16/fp32 values widen exactly).            */
 /* ------------------------------------------------------------------------ */
 int oracle_gated_lora_linear_f64(const double *x, const double *W,
@@ -159,11 +161,11 @@ static int32_t race_f64(const double *w, const float *u, int64_t V, double *marg
 
 /* ------------------------------------------------------------------------ */
 /* Block verifier (Psi-Spec linear sampler, verification half).             */
-/* [Explainer] "The Psi-Spec Sampler": draft a block in parallel, then      */
-/* speculative-decoding-style rejection sampling against the AR model       */
-/* accepts the longest valid prefix; the AR output distribution is kept     */
-/* exactly.  [Article] "What 'lossless' means here": the AR model rejects   */
-/* or adjusts candidates.                                                   */
+/* [Explainer] "The Psi-Spec Sampler": a block drafted in parallel is       */
+/* checked against the AR model by rejection sampling (as in speculative    */
+/* decoding); drafts are kept up to the first rejection and the emitted     */
+/* tokens follow the AR model's distribution.  [Article] "What 'lossless'   */
+/* means here": the AR model has the final say over every draft.            */
 /*                                                                          */
 /* p_logits [Bn,Kp,V] (AR, Kp = K or K+1), q_logits [Bn,K,V] (draft),       */
 /* draft [Bn,K], u_acc [Bn,K] in [0,1), u_res [Bn,V] in (0,1).              */
