@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch ops eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--grouping", choices=["layer", "all", "single"], default="layer",
+                    help="layer: [q,k,v] [o] [gate,up] [down], one persistent launch each (the "
+                         "layer's data dependencies); all: the 7 projections in one launch; "
+                         "single: one launch per projection")
     return ap.parse_args()
 
 
@@ -143,20 +147,31 @@ def dist_setup(n_gpus):
     return ws, rank, local
 
 
+GROUPINGS = {"layer": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
+             "all": [["q", "k", "v", "o", "gate", "up", "down"]],
+             "single": [["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]]}
+
+
 class Step:
     """All inputs, outputs and workspaces of one step, resident on the device."""
 
-    def __init__(self, batch, sigma, device):
+    def __init__(self, batch, sigma, device, grouping="layer"):
         import torch
         from lossless_draft_verify_gated_b300 import binding, inputs
         self.batch, self.device = batch, device
         self.M = 2 * BLOCK * batch
         self.layer = inputs.llama3_layer(self.M, rank=RANK, alpha=ALPHA, block=BLOCK, device=device)
-        self.ys = [torch.empty((self.M, p.W.shape[0]), dtype=torch.bfloat16, device=device)
-                   for _, p in self.layer]
-        self.wss = [torch.empty(max(binding.uno_gated_lora_linear_workspace(self.M, p.W.shape[1],
-                                                                          p.W.shape[0], RANK, 1), 256),
-                                dtype=torch.uint8, device=device) for _, p in self.layer]
+        by_name = dict(self.layer)
+        self.ys = {n: torch.empty((self.M, p.W.shape[0]), dtype=torch.bfloat16, device=device)
+                   for n, p in self.layer}
+        self.groups = []
+        for names in GROUPINGS[grouping]:
+            probs = [(by_name[n].x, by_name[n].W, by_name[n].A, by_name[n].B, by_name[n].gate,
+                      by_name[n].alpha, self.ys[n]) for n in names]
+            shapes = [(p[0].shape[1], p[1].shape[0], p[2].shape[0]) for p in probs]
+            ws = torch.empty(binding.uno_gated_lora_linear_batched_workspace(shapes, self.M, 1),
+                             dtype=torch.uint8, device=device)
+            self.groups.append((probs, ws))
         vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=device)
         self.p, self.q, self.ua, self.ur = vp.p_logits, vp.q_logits, vp.u_accept, vp.u_resample
         # drafts: the linear sampler's drafting half, a single token drawn from q at each position
@@ -168,18 +183,18 @@ class Step:
         self.vws = torch.empty(binding.uno_verify_block_workspace(batch, BLOCK, BLOCK, VOCAB),
                                dtype=torch.uint8, device=device)
         self.n_gate1 = int(self.layer[0][1].gate.sum())
+        # kernels of this library per step: one persistent GEMM per group, two for the verifier
+        self.launches_per_step = len(self.groups) + 2
 
     def projections(self):
         from lossless_draft_verify_gated_b300 import binding
-        for (_, p), y, ws in zip(self.layer, self.ys, self.wss):
-            binding.uno_gated_lora_linear(p.x, p.W, p.A, p.B, p.gate, p.alpha, y=y, workspace=ws)
+        for probs, ws in self.groups:
+            binding.uno_gated_lora_linear_batched(probs, workspace=ws)
 
     def verify(self):
         from lossless_draft_verify_gated_b300 import binding
         binding.uno_verify_block(self.p, self.q, self.draft, self.ua, self.ur, out=self.vout,
                                  workspace=self.vws)
-
-    launches_per_step = 7 * 2 + 2  # down + main GEMM per projection, stats + finish verifier
 
 
 def run_uno(args):
@@ -189,7 +204,7 @@ def run_uno(args):
     from lossless_draft_verify_gated_b300 import binding
     binding.lib()
     hbm, tflops, peak_kind = peaks()
-    st = Step(args.batch, args.sigma, dev)
+    st = Step(args.batch, args.sigma, dev, args.grouping)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
 
     # CUDA graphs of the two halves of the step (launch overhead off the clock)
@@ -273,16 +288,17 @@ def run_uno(args):
                    "rows_per_projection": st.M, "verified_tokens_per_step": tokens,
                    "l2": "flushed before every step (2x L2 write, outside the timed events)",
                    "launch": "CUDA graph per half-step" if g_proj is not None else "eager",
+                   "grouping": args.grouping + ": " + " | ".join(",".join(g) for g in GROUPINGS[args.grouping]),
                    "parallelism": f"dp{ws} (independent replicas, no collective)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "gated-LoRA projections of the layer (7 x [down GEMM + fused main GEMM])",
+                     "kernel": f"gated-LoRA projections of the layer ({len(st.groups)} persistent grouped GEMM launch(es))",
                      "peak_source": peak_kind, "algorithmic_bytes": by, "algorithmic_flops": fl,
                      "ms": round(ms_proj, 5)},
         "verifier": {"ms": round(ms_ver, 5), "bytes": vb,
                      "achieved_gbs": round(vb / (ms_ver / 1e3) / 1e9, 2),
                      "frac_hbm": round(vb / (ms_ver / 1e3) / 1e9 / hbm, 4)},
-        "gpu_launches": Step.launches_per_step * K,
+        "gpu_launches": st.launches_per_step * K,
         "wall_s": round(wall, 3),
     }
     out["clocks"] = clk.summary()
@@ -302,9 +318,12 @@ def e2e(st, dev, steps):
     the verified tokens back."""
     import torch
     host = {}
+    seen = set()
     for i, (_, p) in enumerate(st.layer):
-        host[f"x{i}"] = (p.x.cpu().pin_memory(), p.x)
-        host[f"g{i}"] = (p.gate.cpu().pin_memory(), p.gate)
+        for tag, t in (("x", p.x), ("g", p.gate)):
+            if t.data_ptr() not in seen:  # q/k/v and gate/up share their input; one gate tensor
+                seen.add(t.data_ptr())
+                host[f"{tag}{i}"] = (t.cpu().pin_memory(), t)
     for k in ("p", "q", "draft", "ua", "ur"):
         t = getattr(st, k)
         host[k] = (t.cpu().pin_memory(), t)

@@ -116,6 +116,46 @@ int uno_gated_lora_linear(const void *x, const void *W, const void *A,
                           size_t ws_bytes, uno_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Grouped gated-LoRA projections: up to UNO_MAX_LORA_PROBLEMS projections
+ * that share the row count M (for instance the q/k/v/o/gate/up/down
+ * projections of one transformer layer, each with its own input, weights,
+ * adapter and gate) computed by ONE persistent kernel launch.  Each problem
+ * follows exactly the definition of uno_gated_lora_linear above, with the
+ * same error bound.  The schedule splits the concatenated K loops of all
+ * problems evenly over the SMs (so small projections leave no SM idle); a
+ * K loop cut between two CTAs is summed in a fixed order, so results are
+ * deterministic for a given group, but a problem computed alone may be cut
+ * elsewhere and differ in the last bits.  uno_gated_lora_linear is this
+ * call with n = 1.
+ *   problems  HOST array of n descriptors (device pointers inside)
+ *   M         rows of every x, gate and y
+ *   workspace at least uno_gated_lora_linear_batched_workspace(...) bytes,
+ *             256-byte aligned, contents ignored on entry.
+ * Requirements: 1 <= n <= UNO_MAX_LORA_PROBLEMS; per problem as above.
+ * ------------------------------------------------------------------------- */
+#define UNO_MAX_LORA_PROBLEMS 8
+
+typedef struct {
+    const void *x;       /* [M, d_in]      activations (dtype)                */
+    const void *W;       /* [d_out, d_in]  theta_AR (dtype)                   */
+    const void *A;       /* [rank, d_in]   theta_Delta down-projection (dtype)*/
+    const void *B;       /* [d_out, rank]  theta_Delta up-projection (dtype)  */
+    const uint8_t *gate; /* [M]            1 = draft row, 0 = verification row */
+    void *y;             /* [M, d_out]     output (dtype)                     */
+    int64_t d_in;
+    int64_t d_out;
+    int64_t rank;
+    float alpha;
+} uno_lora_problem;
+
+size_t uno_gated_lora_linear_batched_workspace(int n, const uno_lora_problem *problems,
+                                               int64_t M, int dtype);
+
+int uno_gated_lora_linear_batched(int n, const uno_lora_problem *problems, int64_t M,
+                                  int dtype, void *workspace, size_t ws_bytes,
+                                  uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Block verifier (Psi-Spec linear sampler, verification half).
  * ("Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
  *  aifromscratch.in, "The Psi-Spec Sampler"; "Uno Uses Discrete Diffusion to

@@ -48,6 +48,17 @@ SIGNATURES = {
     "uno_version": (_I, []),
 }
 
+
+
+class LoraProblemC(ctypes.Structure):
+    """uno_lora_problem (include/uno.h)."""
+    _fields_ = [("x", _P), ("W", _P), ("A", _P), ("B", _P), ("gate", _P), ("y", _P),
+                ("d_in", _I64), ("d_out", _I64), ("rank", _I64), ("alpha", ctypes.c_float)]
+
+
+SIGNATURES["uno_gated_lora_linear_batched_workspace"] = (_SZ, [_I, _P, _I64, _I])
+SIGNATURES["uno_gated_lora_linear_batched"] = (_I, [_I, _P, _I64, _I, _P, _SZ, _P])
+
 _lib = None
 
 
@@ -126,6 +137,42 @@ def uno_gated_lora_linear(x, W, A, B, gate, alpha, *, y=None, workspace=None, st
                                      workspace.numel(), _stream(stream))
     _check("uno_gated_lora_linear", rc)
     return y
+
+
+def _problems(problems):
+    arr = (LoraProblemC * len(problems))()
+    for i, (x, W, A, B, gate, alpha, y) in enumerate(problems):
+        for t in (x, W, gate, y) + ((A, B) if A.numel() else ()):
+            _dptr(t)  # device and contiguity checks
+        arr[i] = LoraProblemC(x.data_ptr(), W.data_ptr(), A.data_ptr() if A.numel() else 0,
+                              B.data_ptr() if B.numel() else 0, gate.data_ptr(), y.data_ptr(),
+                              x.shape[1], W.shape[0], A.shape[0], float(alpha))
+    return arr
+
+
+def uno_gated_lora_linear_batched_workspace(shapes, M, dtype) -> int:
+    """shapes: list of (d_in, d_out, rank)."""
+    dt = _DT[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    arr = (LoraProblemC * len(shapes))()
+    for i, (di, do, r) in enumerate(shapes):
+        arr[i] = LoraProblemC(0, 0, 0, 0, 0, 0, di, do, r, 1.0)
+    return int(lib().uno_gated_lora_linear_batched_workspace(len(shapes), ctypes.cast(arr, _P), M, dt))
+
+
+def uno_gated_lora_linear_batched(problems, *, workspace=None, stream=None):
+    """problems: list of (x, W, A, B, gate, alpha, y) tensors, all with the same
+    row count M and dtype.  One persistent kernel computes every y in place."""
+    x0 = problems[0][0]
+    M = x0.shape[0]
+    dt = _DT[x0.dtype]
+    arr = _problems(problems)
+    if workspace is None:
+        shapes = [(p[0].shape[1], p[1].shape[0], p[2].shape[0]) for p in problems]
+        workspace = _workspace(uno_gated_lora_linear_batched_workspace(shapes, M, dt), x0.device)
+    rc = lib().uno_gated_lora_linear_batched(len(problems), ctypes.cast(arr, _P), M, dt,
+                                             _dptr(workspace), workspace.numel(), _stream(stream))
+    _check("uno_gated_lora_linear_batched", rc)
+    return [p[6] for p in problems]
 
 
 def uno_verify_block_workspace(Bn, K, Kp, V) -> int:

@@ -74,24 +74,61 @@ const char* uno_status_string(int code) {
 size_t uno_gated_lora_linear_workspace(int64_t M, int64_t d_in, int64_t d_out, int64_t rank,
                                        int dtype) {
   if (!lora_shape_ok(M, d_in, d_out, rank, dtype)) return 0;
-  return lora_workspace_bytes(M, d_in, d_out, rank, dtype, sm_count());
+  uno_lora_problem p{};
+  p.d_in = d_in;
+  p.d_out = d_out;
+  p.rank = rank;
+  return lora_group_workspace_bytes(1, &p, M, dtype, sm_count());
 }
 
 int uno_gated_lora_linear(const void* x, const void* W, const void* A, const void* B,
                           const uint8_t* gate, int64_t M, int64_t d_in, int64_t d_out,
                           int64_t rank, float alpha, int dtype, void* y, void* workspace,
                           size_t ws_bytes, uno_stream_t stream) {
+  uno_lora_problem p{};
+  p.x = x;
+  p.W = W;
+  p.A = A;
+  p.B = B;
+  p.gate = gate;
+  p.y = y;
+  p.d_in = d_in;
+  p.d_out = d_out;
+  p.rank = rank;
+  p.alpha = alpha;
+  return uno_gated_lora_linear_batched(1, &p, M, dtype, workspace, ws_bytes, stream);
+}
+
+size_t uno_gated_lora_linear_batched_workspace(int n, const uno_lora_problem* problems, int64_t M,
+                                               int dtype) {
+  if (n < 1 || n > UNO_MAX_LORA_PROBLEMS || !problems) return 0;
+  for (int i = 0; i < n; ++i)
+    if (!lora_shape_ok(M, problems[i].d_in, problems[i].d_out, problems[i].rank, dtype)) return 0;
+  return lora_group_workspace_bytes(n, problems, M, dtype, sm_count());
+}
+
+int uno_gated_lora_linear_batched(int n, const uno_lora_problem* problems, int64_t M, int dtype,
+                                  void* workspace, size_t ws_bytes, uno_stream_t stream) {
   if (dtype != UNO_F32 && dtype != UNO_BF16) return UNO_ERR_UNSUPPORTED;
-  if (!lora_shape_ok(M, d_in, d_out, rank, dtype)) return UNO_ERR_ARG;
-  if (!(alpha == alpha) || alpha == INFINITY || alpha == -INFINITY) return UNO_ERR_ARG;
+  if (n < 1 || n > UNO_MAX_LORA_PROBLEMS || !problems) return UNO_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    const uno_lora_problem& p = problems[i];
+    if (!lora_shape_ok(M, p.d_in, p.d_out, p.rank, dtype)) return UNO_ERR_ARG;
+    if (!(p.alpha == p.alpha) || p.alpha == INFINITY || p.alpha == -INFINITY) return UNO_ERR_ARG;
+  }
   if (M == 0) return UNO_OK;
-  if (!x || !W || !gate || !y || !workspace) return UNO_ERR_ARG;
-  if (rank > 0 && (!A || !B)) return UNO_ERR_ARG;
-  if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (rank > 0 && (!aligned16(A) || !aligned16(B))))
-    return UNO_ERR_ALIGN;
+  for (int i = 0; i < n; ++i) {
+    const uno_lora_problem& p = problems[i];
+    if (!p.x || !p.W || !p.gate || !p.y) return UNO_ERR_ARG;
+    if (p.rank > 0 && (!p.A || !p.B)) return UNO_ERR_ARG;
+    if (!aligned16(p.x) || !aligned16(p.W) || !aligned16(p.y) ||
+        (p.rank > 0 && (!aligned16(p.A) || !aligned16(p.B))))
+      return UNO_ERR_ALIGN;
+  }
+  if (!workspace) return UNO_ERR_ARG;
   if (!aligned256(workspace)) return UNO_ERR_WORKSPACE;
-  return launch_gated_lora_linear(x, W, A, B, gate, M, d_in, d_out, rank, alpha, dtype, y,
-                                  workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return launch_lora_group(n, problems, M, dtype, workspace, ws_bytes,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t uno_verify_block_workspace(int64_t Bn, int64_t K, int64_t Kp, int64_t V) {

@@ -40,13 +40,9 @@ cudaError_t launch_draft_sample(const float* logits, const float* u, int64_t R,
                                 cudaStream_t st);
 
 // -------------------------------------------------------------- projection
-struct LoraPlan;  // defined in gemm.cu
-size_t lora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int64_t rank,
-                            int dtype, int sms);
-int launch_gated_lora_linear(const void* x, const void* W, const void* A,
-                             const void* B, const uint8_t* gate, int64_t M,
-                             int64_t d_in, int64_t d_out, int64_t rank,
-                             float alpha, int dtype, void* y, void* ws,
-                             size_t ws_bytes, cudaStream_t st);
+constexpr int kMaxLoraProblems = UNO_MAX_LORA_PROBLEMS;
+size_t lora_group_workspace_bytes(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms);
+int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, void* ws,
+                      size_t ws_bytes, cudaStream_t st);
 
 }  // namespace uno

@@ -181,19 +181,44 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
-  // 1. Row normalisers of this sequence from the statistics partials.
-  for (int64_t j = tid; j < per_seq; j += kThreads) {
-    const float2* pp = part + (b * per_seq + j) * splits;
-    MS t{-INFINITY, 0.f};
-    for (int s = 0; s < splits; ++s) {
-      const float2 v = pp[s];
-      t = ms_merge(t, MS{v.x, v.y});
+  // 1. Row normalisers of this sequence from the statistics partials: one
+  //    warp per row, lanes over the chunk partials, loads of four rows in
+  //    flight at once.
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int64_t j0 = int64_t(warp) * 4; j0 < per_seq; j0 += kWarps * 4) {
+      MS t[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) t[r] = MS{-INFINITY, 0.f};
+      for (int s0 = 0; s0 < splits; s0 += 64) {
+        float2 v[4][2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int s = s0 + lane + 32 * h;
+            const int64_t j = j0 + r;
+            v[r][h] = (j < per_seq && s < splits) ? part[(b * per_seq + j) * splits + s]
+                                                  : make_float2(-INFINITY, 0.f);
+          }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) t[r] = ms_merge(t[r], MS{v[r][h].x, v[r][h].y});
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const MS m = warp_merge(t[r]);
+        const int64_t j = j0 + r;
+        if (lane == 0 && j < per_seq) {
+          const bool bad = isnan(m.s) || !(m.m > -INFINITY) || !(m.m < INFINITY) || !(m.s > 0.f);
+          if (bad) atomicOr(&s_bad, 2);
+          s_m[j] = m.m;
+          s_lz[j] = m.m + logf(m.s);
+          s_iz[j] = 1.0f / m.s;
+        }
+      }
     }
-    const bool bad = isnan(t.s) || !(t.m > -INFINITY) || !(t.m < INFINITY) || !(t.s > 0.f);
-    if (bad) atomicOr(&s_bad, 2);
-    s_m[j] = t.m;
-    s_lz[j] = t.m + logf(t.s);
-    s_iz[j] = 1.0f / t.s;
   }
   // 2. Draft ids and acceptance flags.
   for (int64_t i = tid; i < K; i += kThreads) {
@@ -261,13 +286,28 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const int64_t v0 = int64_t(split) * race_chunk;
   const int64_t v1 = min(V, v0 + race_chunk);
   Cand cr{0.f, -1}, cp{-1.f, -1};
-  for (int64_t v = v0 + tid; v < v1; v += kThreads) {
-    const float e = -logf(ub[v]);
-    const float pv = expf(pr[v] - mp) * izp;
-    cp = cand_best(cp, Cand{pv / e, int(v)});
-    if (residual) {
-      const float rv = pv - expf(qr[v] - mq) * izq;
-      if (rv > 0.f) cr = cand_best(cr, Cand{rv / e, int(v)});
+  constexpr int kRaceUnroll = 4;
+  for (int64_t v = v0 + tid; v < v1; v += int64_t(kThreads) * kRaceUnroll) {
+    float uu[kRaceUnroll], lp[kRaceUnroll], lq[kRaceUnroll];
+#pragma unroll
+    for (int i = 0; i < kRaceUnroll; ++i) {
+      const int64_t vi = v + int64_t(i) * kThreads;
+      const bool in = vi < v1;
+      uu[i] = in ? ub[vi] : 0.5f;
+      lp[i] = in ? pr[vi] : -INFINITY;
+      lq[i] = (in && residual) ? qr[vi] : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < kRaceUnroll; ++i) {
+      const int64_t vi = v + int64_t(i) * kThreads;
+      if (vi >= v1) break;
+      const float e = -logf(uu[i]);
+      const float pv = expf(lp[i] - mp) * izp;
+      cp = cand_best(cp, Cand{pv / e, int(vi)});
+      if (residual) {
+        const float rv = pv - expf(lq[i] - mq) * izq;
+        if (rv > 0.f) cr = cand_best(cr, Cand{rv / e, int(vi)});
+      }
     }
   }
   cr = warp_best(cr);
@@ -289,29 +329,47 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       rpart[b * race_splits + split] = RacePart{cr.s, cr.v, cp.s, cp.v};
       __threadfence();
       last = atomicAdd(&counter[b], 1) == race_splits - 1;
-      if (last) {
-        __threadfence();
-        cr = Cand{0.f, -1};
-        cp = Cand{-1.f, -1};
-        for (int s = 0; s < race_splits; ++s) {
-          const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
-          cr = cand_best(cr, Cand{__int_as_float(t.x), t.y});
-          cp = cand_best(cp, Cand{__int_as_float(t.z), t.w});
-        }
-        counter[b] = 0;
-      }
     }
     s_last = last;
-    if (last) {
-      const int tok = (residual && cr.v >= 0) ? cr.v : cp.v;
-      n_acc[b] = n;
-      n_emit[b] = n + 1;
-      status[b] = UNO_SEQ_OK;
-      s_n = tok;
-    }
   }
   __syncthreads();
   if (!s_last) return;
+  if (race_splits > 1) {
+    // The last CTA of the sequence merges every chunk's winner (loads spread
+    // over the block, then the same warp/block reduction).
+    __threadfence();
+    cr = Cand{0.f, -1};
+    cp = Cand{-1.f, -1};
+    for (int s = tid; s < race_splits; s += kThreads) {
+      const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
+      cr = cand_best(cr, Cand{__int_as_float(t.x), t.y});
+      cp = cand_best(cp, Cand{__int_as_float(t.z), t.w});
+    }
+    cr = warp_best(cr);
+    cp = warp_best(cp);
+    __syncthreads();
+    if ((tid & 31) == 0) {
+      s_cr[tid >> 5] = cr;
+      s_cp[tid >> 5] = cp;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      cr = s_cr[0];
+      cp = s_cp[0];
+      for (int w = 1; w < kWarps; ++w) {
+        cr = cand_best(cr, s_cr[w]);
+        cp = cand_best(cp, s_cp[w]);
+      }
+      counter[b] = 0;
+    }
+  }
+  if (tid == 0) {
+    n_acc[b] = n;
+    n_emit[b] = n + 1;
+    status[b] = UNO_SEQ_OK;
+    s_n = (residual && cr.v >= 0) ? cr.v : cp.v;
+  }
+  __syncthreads();
   const int tok = s_n;
   for (int64_t i = tid; i <= K; i += kThreads)
     out[i] = i < n ? draft[b * K + i] : (i == n ? tok : -1);

@@ -110,11 +110,22 @@ def lora_problem(M: int, d_in: int, d_out: int, rank: int, alpha: float, *,
 
 def llama3_layer(M: int, *, rank: int = 128, alpha: float = 256.0, block: int = 16,
                  seed: int = BASE_SEED, dtype=torch.bfloat16, device="cpu"):
-    """The 7 projections of one Llama-3-8B-shaped layer at M rows."""
-    return [(n, lora_problem(M, di, do, rank, alpha, dtype=dtype, block=block, seed=seed,
-                             name=f"llama3.{n}", x_name=f"llama3.{LLAMA3_8B_INPUT_OF[n]}",
-                             device=device))
-            for n, di, do in LLAMA3_8B_PROJECTIONS]
+    """The 7 projections of one Llama-3-8B-shaped layer at M rows.  Projections
+    that read the same layer input (q/k/v, gate/up) share one x tensor, and all
+    share one gate tensor, as in the layer itself."""
+    out, xs, gate = [], {}, None
+    for n, di, do in LLAMA3_8B_PROJECTIONS:
+        pr = lora_problem(M, di, do, rank, alpha, dtype=dtype, block=block, seed=seed,
+                          name=f"llama3.{n}", x_name=f"llama3.{LLAMA3_8B_INPUT_OF[n]}", device=device)
+        key = LLAMA3_8B_INPUT_OF[n]
+        if key in xs:
+            pr.x = xs[key]  # same seed and name: identical values, one tensor
+        else:
+            xs[key] = pr.x
+        gate = pr.gate if gate is None else gate
+        pr.gate = gate
+        out.append((n, pr))
+    return out
 
 
 @dataclass

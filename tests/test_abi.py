@@ -106,3 +106,29 @@ def test_verify_argument_errors(L):
     assert call(Bn=0) == 0
     assert L.uno_draft_sample(None, None, 4, 10, None, None, None) == -1
     assert L.uno_draft_sample(None, None, 0, 10, None, None, None) == 0
+
+
+def test_batched_argument_errors(L):
+    from lossless_draft_verify_gated_b300 import binding
+    P = binding.LoraProblemC
+
+    def arr(*ps):
+        a = (P * len(ps))(*ps)
+        return ctypes.cast(a, ctypes.c_void_p), a
+
+    good = P(256, 256, 256, 256, 256, 256, 64, 64, 16, 32.0)
+    a, keep = arr(good, good)
+    ws = ctypes.c_void_p(256)
+    assert L.uno_gated_lora_linear_batched(0, a, 4, 1, ws, 1 << 20, None) == -1
+    assert L.uno_gated_lora_linear_batched(9, a, 4, 1, ws, 1 << 20, None) == -1
+    bad = P(256, 256, 256, 256, 256, 256, 60, 64, 16, 32.0)  # d_in not a multiple of 8
+    a2, keep2 = arr(good, bad)
+    assert L.uno_gated_lora_linear_batched(2, a2, 4, 1, ws, 1 << 20, None) == -1
+    mis = P(264, 256, 256, 256, 256, 256, 64, 64, 16, 32.0)
+    a3, keep3 = arr(mis)
+    assert L.uno_gated_lora_linear_batched(1, a3, 4, 1, ws, 1 << 20, None) == -2
+    assert L.uno_gated_lora_linear_batched(2, a, 4, 1, ws, 16, None) == -4
+    assert L.uno_gated_lora_linear_batched(2, a, 0, 1, ws, 16, None) == 0
+    w1 = binding.uno_gated_lora_linear_batched_workspace([(4096, 4096, 128)] * 7, 32, 1)
+    w2 = binding.uno_gated_lora_linear_workspace(32, 4096, 4096, 128, 1)
+    assert w1 > w2 > 0

@@ -111,3 +111,61 @@ def test_deterministic():
 def test_no_device_error_flag():
     from lossless_draft_verify_gated_b300 import uno_device_error
     assert uno_device_error() == 0
+
+
+def _batched(problems_pr, dtype=torch.bfloat16):
+    from lossless_draft_verify_gated_b300 import uno_gated_lora_linear_batched
+    d = "cuda"
+    probs = []
+    for pr in problems_pr:
+        y = torch.empty((pr.x.shape[0], pr.W.shape[0]), dtype=dtype, device=d)
+        probs.append((pr.x.to(d), pr.W.to(d), pr.A.to(d), pr.B.to(d), pr.gate.to(d), pr.alpha, y))
+    ys = uno_gated_lora_linear_batched(probs)
+    torch.cuda.synchronize()
+    return ys
+
+
+@pytest.mark.parametrize("M", [32, 16])
+def test_batched_llama3_layer_decode(M):
+    """All 7 projections of the Llama-3-8B-shaped layer in one persistent launch."""
+    layer = inputs.llama3_layer(M, rank=128, alpha=256.0, block=16 if M >= 32 else 8)
+    ys = _batched([pr for _, pr in layer])
+    for (name, pr), y in zip(layer, ys):
+        assert gemm_err(y, _ref(pr)) <= GEMM_TOL, name
+
+
+def test_batched_llama3_layer_large_m_sampled():
+    M = 2048
+    layer = inputs.llama3_layer(M, rank=128, alpha=256.0, block=16)
+    ys = _batched([pr for _, pr in layer])
+    rows = torch.randperm(M, generator=inputs.generator("rows.batched"))[:32]
+    for (name, pr), y in zip(layer, ys):
+        assert gemm_err(y[rows.cuda()], _ref(pr, rows)) <= GEMM_TOL, name
+
+
+@pytest.mark.parametrize("M", [24, 300])
+def test_batched_mixed_ranks_and_shapes(M):
+    """Rank 0 next to rank 8, 24 and 128, ragged d_in/d_out, swap and non-swap paths."""
+    shapes = [(200, 136, 24, 48.0), (512, 1000, 0, 1.0), (64, 520, 128, 256.0), (1032, 72, 8, 16.0)]
+    prs = [inputs.lora_problem(M, di, do, r, a, block=4, name=f"mix.{M}.{i}")
+           for i, (di, do, r, a) in enumerate(shapes)]
+    ys = _batched(prs)
+    for pr, y in zip(prs, ys):
+        assert gemm_err(y, _ref(pr)) <= GEMM_TOL
+
+
+def test_batched_fp32():
+    prs = [inputs.lora_problem(16, 256, 256, 16, 32.0, dtype=torch.float32, block=4, name=f"f32.{i}")
+           for i in range(3)]
+    ys = _batched(prs, dtype=torch.float32)
+    for pr, y in zip(prs, ys):
+        assert y.dtype == torch.float32
+        assert gemm_err(y, _ref(pr)) <= GEMM_TOL
+
+
+def test_batched_deterministic():
+    layer = inputs.llama3_layer(32, seed=7)
+    a = _batched([pr for _, pr in layer])
+    b = _batched([pr for _, pr in layer])
+    for ya, yb in zip(a, b):
+        assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
