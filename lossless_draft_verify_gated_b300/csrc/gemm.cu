@@ -7,29 +7,37 @@
 // theta_Delta; verification rows (gate 0) get theta_AR alone.
 //
 // One persistent, warp-specialised kernel computes a whole group of
-// projections (for example the seven projections of a transformer layer):
+// projections (for example the seven projections of a transformer layer).
 //
-//   * Work is a flat sequence of 64-wide K-blocks: first the down-projection
-//     tiles of every problem, T = bf16(gate * alpha/rank * x.A^T), then the
-//     main tiles, each made of its d_in/64 base K-blocks followed by its
-//     rank/64 adapter K-blocks (A-operand B, B-operand T).  The adapter
-//     therefore accumulates into the same TMEM accumulator as x.W^T: W is
-//     streamed from HBM once and y is written once.
-//   * CTA c of G takes the contiguous K-block range [c*Tot/G, (c+1)*Tot/G)
-//     ("stream-K"), so every SM streams the same number of K-blocks whatever
-//     the shapes.  A tile cut by range boundaries is finished by the last of
-//     its CTAs to arrive, which sums the partials in CTA order
-//     (deterministic results, nobody waits).
-//   * A main tile's adapter K-blocks need T: the producer waits (bounded) on
-//     the flag its down tile sets.  Down tiles come first in the sequence and
-//     never wait, so the wait always ends; the launch is cooperative so all
-//     CTAs are resident.
+// Work is split into 64-wide K-blocks, in two sections:
+//   * the down section: tiles of T = bf16(gate * alpha/rank * x.A^T), one
+//     run of tiles per problem with a nonzero rank;
+//   * the main section: tiles of y, each a flat run of rank/64 adapter
+//     K-blocks (A-operand B, B-operand T) followed by d_in/64 base K-blocks
+//     (x.W^T).  The adapter accumulates into the same TMEM accumulator as
+//     x.W^T, so W is streamed from HBM once and y is written once.
+// CTA c owns a contiguous range of each section (stream-K): the down section
+// is spread over enough CTAs that each does a few K-blocks, first thing, so
+// T is complete early; the main ranges are sized so that every CTA streams
+// the same number of K-blocks in total.  Inside a range piece a CTA runs the
+// base K-blocks first and the adapter K-blocks last, so T is needed only at
+// the end of a piece.
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA (cp.async.bulk.tensor, 128-byte
-// swizzle) into a STAGES-deep shared-memory ring; warp 1 owns TMEM and its
-// lane 0 issues tcgen05.mma (M=128, N=bn, K=16, bf16 -> fp32) into one of two
-// TMEM accumulators; warps 2-5 drain the other accumulator (tcgen05.ld) and
-// store y, T or split-K partials, overlapping the next tile's MMAs.
+// A tile cut between CTAs is finished by the CTA that owns its first K-block
+// (for that CTA it is always the last piece of the section).  The other
+// owners hold their piece of the tile as the first piece of their range:
+// they leave it as an fp32 partial and raise a flag.  The finisher adds the
+// partials in CTA order to its own accumulator (deterministic).  Every wait
+// points at a CTA with a higher index or at a flag raised before any wait of
+// its raiser, so waits always end; the launch is cooperative so all CTAs are
+// resident.  A main tile's adapter K-blocks wait for the flags of the T
+// tiles they read.
+//
+// Roles (192 threads): warp 0 lane 0 issues TMA (cp.async.bulk.tensor,
+// 128-byte swizzle) into a STAGES-deep shared-memory ring; warp 1 owns TMEM
+// and its lane 0 issues tcgen05.mma (M=128, N=bn, K=16, bf16 -> fp32) into
+// one of two TMEM accumulators; warps 2-5 drain the other accumulator
+// (tcgen05.ld) and store y, T or partials, overlapping the next piece's MMAs.
 // Decode-sized M (<= 256 token rows) swaps the operands so that the weights
 // fill the 128-row MMA side and the tokens are N.
 // Every wait is bounded (2 s): a timeout sets the device error word and the
@@ -58,6 +66,8 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 2 * kMaxLoraProblems;
+constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
+constexpr int kDown = 0, kMain = 1;
 
 enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, kMapsPerProblem = 5 };
 
@@ -65,14 +75,15 @@ struct Maps {
   CUtensorMap m[kMaxLoraProblems][kMapsPerProblem];
 };
 
+// A run of equally shaped tiles of one problem inside a section.
 struct Phase {
-  int64_t kb_start;  // first K-block of the phase in the global sequence
+  int64_t kb_start;  // first K-block of the phase in its section
   int tiles;
-  int tiles_a;       // tiles along the A-operand rows
+  int tiles_a;       // tiles along the A-operand rows (tile = tb * tiles_a + ta)
   int nkb;           // K-blocks per tile
-  int nkb_base;      // of which over d_in; the rest are adapter K-blocks
+  int na;            // of which adapter K-blocks, first in the flat order (0 in the down section)
   int prob;
-  int down;          // 1: T = gate*scale*x.A^T;  0: y = x.W^T + T.B^T
+  int down;          // 1: T = gate*scale*x.A^T;  0: y = T.B^T + x.W^T
   int bn;            // MMA N (B-operand rows per tile)
 };
 
@@ -83,59 +94,60 @@ struct Prob {
   float scale;
   int d_out;
   int r;
-  int flag_base;
-  int down_tiles;
+  int tflag0;  // first T-ready flag of the problem
+  int ttiles;  // T tiles of the problem
 };
 
 struct Params {
   Phase ph[kMaxPhases];
   Prob pb[kMaxLoraProblems];
-  int nph;
+  int ph0[2], ph1[2];  // section s holds phases [ph0[s], ph1[s])
   int swap;
   int M;
   int out_f32;
   int grid;
   int bnmax;
-  int64_t total;
+  int64_t lo[2][kMaxGrid + 1];  // CTA c owns K-blocks [lo[s][c], lo[s][c+1]) of section s
   float* partial;  // [grid][2][bnmax * 128], layout [column/4][row][4]
-  int* counters;   // [grid]
-  int* flags;      // [sum of down tiles]
+  int* ready;      // [2][grid]: the first piece of CTA c in section s left its partial
+  int* tflag;      // [T tiles]: the rows of T of the tile are written
 };
 
-// Tuning constants: K-blocks per pipeline stage (a stage holds KPS consecutive
-// 64-wide K slices, so a weight row is read as KPS*128 contiguous bytes) and
-// the shared-memory budget of the ring.
-#ifndef UNO_KPS_DECODE
-#define UNO_KPS_DECODE 1
-#endif
-#ifndef UNO_MAX_STAGES
-#define UNO_MAX_STAGES 8
-#endif
-constexpr uint32_t kRingBudget = 200 * 1024;
+// Shared memory: a ring of one K-block per stage (A sub-tile, then B
+// sub-tile) and, for decode-sized tiles (N <= 64), a staging area into which a
+// finisher bulk-copies its contributors' partials.
+constexpr int kMaxStages = 10;
+constexpr uint32_t kStagingBytes = 96 * 1024;
 
 template <int BNMAX>
-__host__ __device__ constexpr int kps_for() {
-  return BNMAX <= 64 ? UNO_KPS_DECODE : 1;
+__host__ __device__ constexpr bool pre_merge() {
+  return BNMAX <= 64;
 }
-template <int BNMAX, int KPS>
+template <int BNMAX>
+__host__ __device__ constexpr uint32_t staging_bytes() {
+  return pre_merge<BNMAX>() ? kStagingBytes : 0;
+}
+template <int BNMAX>
+__host__ __device__ constexpr int staging_slots() {  // partials the staging area holds at once
+  return pre_merge<BNMAX>() ? int(kStagingBytes / (uint32_t(BNMAX) * 128 * 4)) : 0;
+}
+template <int BNMAX>
 __host__ __device__ constexpr uint32_t stage_bytes() {
-  return uint32_t(KPS) * uint32_t(kBM * kBK * 2 + BNMAX * kBK * 2);
+  return uint32_t(kBM * kBK * 2 + BNMAX * kBK * 2);
 }
-template <int BNMAX, int KPS>
+template <int BNMAX>
 __host__ __device__ constexpr int stages_for() {
-  return int(kRingBudget / stage_bytes<BNMAX, KPS>()) < UNO_MAX_STAGES
-             ? int(kRingBudget / stage_bytes<BNMAX, KPS>())
-             : UNO_MAX_STAGES;
+  return int((220 * 1024 - staging_bytes<BNMAX>()) / stage_bytes<BNMAX>()) < kMaxStages
+             ? int((220 * 1024 - staging_bytes<BNMAX>()) / stage_bytes<BNMAX>())
+             : kMaxStages;
 }
-template <int BNMAX, int KPS>
+// Barriers and the TMEM slot, then a copy of the kernel parameters.
+constexpr uint32_t kBarrierBytes = 256;
+constexpr uint32_t kParamsBytes = (uint32_t(sizeof(Params)) + 15u) & ~15u;
+template <int BNMAX>
 __host__ __device__ constexpr uint32_t smem_bytes_for() {
-  return uint32_t(stages_for<BNMAX, KPS>()) * stage_bytes<BNMAX, KPS>() + 1024 + 256;
-}
-
-__device__ __forceinline__ int64_t range_lo(int c, int G, int64_t T) { return int64_t(c) * T / G; }
-// CTA whose range holds K-block k: the largest c with range_lo(c) <= k.
-__device__ __forceinline__ int cta_of(int64_t k, int G, int64_t T) {
-  return int(((k + 1) * G - 1) / T);
+  return uint32_t(stages_for<BNMAX>()) * stage_bytes<BNMAX>() + staging_bytes<BNMAX>() + kBarrierBytes +
+         kParamsBytes + 1024;
 }
 
 struct Seg {
@@ -143,10 +155,10 @@ struct Seg {
   int64_t tstart, tend, s, e;
 };
 
-__device__ __forceinline__ Seg locate(const Params& P, int64_t k, int64_t hi) {
+__device__ __forceinline__ Seg locate(const Params& P, int sec, int64_t k, int64_t hi) {
   Seg g;
-  int p = 0;
-  while (p + 1 < P.nph && P.ph[p + 1].kb_start <= k) ++p;
+  int p = P.ph0[sec];
+  while (p + 1 < P.ph1[sec] && P.ph[p + 1].kb_start <= k) ++p;
   const Phase& f = P.ph[p];
   g.ph = p;
   g.tile = int((k - f.kb_start) / f.nkb);
@@ -155,6 +167,24 @@ __device__ __forceinline__ Seg locate(const Params& P, int64_t k, int64_t hi) {
   g.s = k;
   g.e = hi < g.tend ? hi : g.tend;
   return g;
+}
+
+// Flat position of the i-th K-block a CTA runs in piece g: base K-blocks
+// first, then the adapter K-blocks (flat positions [tstart, tstart + na)).
+__device__ __forceinline__ int64_t piece_kb(const Seg& g, int na, int64_t i) {
+  const int64_t bs = g.s > g.tstart + na ? g.s : g.tstart + na;
+  const int64_t nb = g.e > bs ? g.e - bs : 0;
+  return i < nb ? bs + i : g.s + (i - nb);
+}
+
+// CTA whose range of section `sec` holds K-block k (ranges may be empty).
+__device__ __forceinline__ int owner_of(const Params& P, int sec, int64_t k) {
+  int a = 0, b = P.grid - 1;
+  while (a < b) {
+    const int m = (a + b + 1) >> 1;
+    if (P.lo[sec][m] <= k) a = m; else b = m - 1;
+  }
+  return a;
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -171,35 +201,111 @@ __device__ __forceinline__ void fence_proxy_async() {
 __device__ __forceinline__ void epi_sync() {  // named barrier of the 4 epilogue warps
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
+// Barrier of the 4 epilogue warps that also ORs `v` over them: every thread
+// gets the same answer.
+__device__ __forceinline__ bool epi_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 __device__ __forceinline__ bool wait_flag(const int* f, uint64_t limit_ns) {
   if (ld_acquire(f)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (!ld_acquire(f)) {
-    __nanosleep(100);
+    __nanosleep(64);
     if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
+// Waits (bounded) until every CTA in [c_from, c_to] whose range of section
+// `sec` is not empty has raised its ready flag.  The flags of up to 16 CTAs
+// are loaded at once (relaxed) and one fence then gives them acquire
+// semantics, so a batch costs one round trip to L2 instead of one per CTA.
+__device__ __forceinline__ bool wait_ready(const Params& P, int sec, int c_from, int c_to,
+                                           uint64_t limit_ns) {
+  const int* flags = P.ready + sec * P.grid;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (int c = c_from; c <= c_to; c += 16) {
+    while (true) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = (c + i <= c_to && P.lo[sec][c + i] < P.lo[sec][c + i + 1]) ? ld_relaxed(flags + c + i) : 1;
+      int ok = 1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ok &= v[i] != 0;
+      if (ok) break;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+      __nanosleep(32);
+    }
+  }
+  fence_acq_rel_gpu();
+  return true;
+}
 
 // Stores 16 consecutive accumulator columns (c0 .. c0+15) of TMEM lane `row`.
+// Must be called by all 32 lanes of the warp (the swap path shuffles).
 __device__ __forceinline__ void store16(const Params& P, const Phase& f, const Prob& pb, int ta,
                                        int tb, int row, int c0, const float (&v)[16]) {
   const int ncols = f.down ? pb.r : pb.d_out;
   __nv_bfloat16* dst16 = static_cast<__nv_bfloat16*>(f.down ? pb.t : pb.y);
   if (P.swap) {
-    // lane = output column n, accumulator column = token m
-    const int n = ta * kBM + row;
-    if (n >= ncols) return;
+    // lane = output column, accumulator column = token.  An 8x8 transpose
+    // by xor-shuffles inside each group of 8 lanes leaves lane 8k+i with 8
+    // consecutive output columns of one token: one 16-byte store per lane.
+    const int lane = row & 31;
+    const int i = lane & 7;
+    const int n = ta * kBM + (row & ~7);  // first output column of this lane group
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int m = tb * f.bn + c0 + j;
-      if (m >= P.M) break;
-      float x = v[j];
-      if (f.down) x *= float(pb.gate[m]) * pb.scale;
-      if (!f.down && P.out_f32)
-        static_cast<float*>(pb.y)[int64_t(m) * ncols + n] = x;
-      else
-        dst16[int64_t(m) * ncols + n] = __float2bfloat16_rn(x);
+    for (int g = 0; g < 2; ++g) {
+      float r[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = v[8 * g + j];
+#pragma unroll
+      for (int sh = 4; sh > 0; sh >>= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j & sh) continue;
+          const float send = (i & sh) ? r[j] : r[j + sh];
+          const float got = __shfl_xor_sync(0xffffffffu, send, sh);
+          if (i & sh) r[j] = got; else r[j + sh] = got;
+        }
+      }
+      const int m = tb * f.bn + c0 + 8 * g + i;  // token of this lane
+      if (m >= P.M || n >= ncols) continue;
+      if (f.down) {
+        const float gs = float(pb.gate[m]) * pb.scale;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[j] *= gs;
+      }
+      if (!f.down && P.out_f32) {
+        float4* d = reinterpret_cast<float4*>(static_cast<float*>(pb.y) + int64_t(m) * ncols + n);
+        d[0] = make_float4(r[0], r[1], r[2], r[3]);
+        d[1] = make_float4(r[4], r[5], r[6], r[7]);
+      } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(r[2 * j], r[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(dst16 + int64_t(m) * ncols + n) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   } else {
     // lane = token m, accumulator column = output column n
@@ -230,33 +336,55 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
   }
 }
 
-template <int BNMAX, int KPS>
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  ptx::tmem_ld_32x32b_x16(taddr, r);
+  ptx::tmem_ld_wait(r);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+template <int BNMAX>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params P) {
-  constexpr int STAGES = stages_for<BNMAX, KPS>();
-  constexpr uint32_t kABytes = kBM * kBK * 2;            // one A sub-tile (128 x 64)
-  constexpr uint32_t kBSub = BNMAX * kBK * 2;            // one B sub-tile slot (BNMAX x 64)
-  constexpr uint32_t kStage = stage_bytes<BNMAX, KPS>();  // KPS A sub-tiles, then KPS B slots
+grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params Pk) {
+  constexpr int STAGES = stages_for<BNMAX>();
+  constexpr uint32_t kABytes = kBM * kBK * 2;       // A sub-tile (128 x 64)
+  constexpr uint32_t kStage = stage_bytes<BNMAX>();  // A sub-tile, then the B slot
   constexpr uint32_t kTmemCols = 2 * BNMAX < 32 ? 32 : 2 * BNMAX;
+  constexpr size_t kSlot = size_t(BNMAX) * kBM;      // floats of one partial slot
+  // Decode-sized tiles: a finisher sums its contributors' partials into
+  // registers while its own last piece is still in the tensor cores.
+  constexpr bool kPreMerge = pre_merge<BNMAX>();
+  constexpr int kSlots = staging_slots<BNMAX>();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStage);
+  float* staging = reinterpret_cast<float*>(smem + STAGES * kStage);  // [kSlots][bn/4][128][4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStage + staging_bytes<BNMAX>());
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2] accumulator ready
   uint64_t* tempty = tfull + 2;      // [2] accumulator drained
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* stg_bar = mma_done + 1;  // staging area filled
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  // The schedule is read with run-time indices all through the kernel: keep a
+  // copy in shared memory rather than in the (small) constant cache.
+  Params* sp = reinterpret_cast<Params*>(reinterpret_cast<uint8_t*>(full) + kBarrierBytes);
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&Pk);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(sp);
+    for (uint32_t i = threadIdx.x; i < sizeof(Params) / 4; i += kThreads) dst[i] = src[i];
+  }
+  const Params& P = *sp;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int G = P.grid;
-  const int64_t lo = range_lo(blockIdx.x, G, P.total);
-  const int64_t hi = range_lo(blockIdx.x + 1, G, P.total);
+  const int cta = blockIdx.x;
 
+  static_assert((2 * STAGES + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
+  static_assert(smem_bytes_for<BNMAX>() <= 227 * 1024, "shared memory per CTA");
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -267,6 +395,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
       ptx::mbar_init(&tempty[a], kEpiThreads / 32);
     }
     ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(stg_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -282,68 +411,68 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      const uint64_t pol_first = ptx::policy_evict_first();
-      const uint64_t pol_last = ptx::policy_evict_last();
       // swap: A = weights (streamed once), B = tokens (reused by every tile);
       // otherwise A = tokens, B = weights, both reused across tiles from L2.
-      const uint64_t polA = P.swap ? pol_first : pol_last;
-      const uint64_t polB = pol_last;
+      const uint64_t polA = P.swap ? ptx::policy_evict_first() : ptx::policy_evict_last();
+      const uint64_t polB = ptx::policy_evict_last();
       uint32_t it = 0;
-      for (int64_t k = lo; k < hi && !*abort_flag;) {
-        const Seg g = locate(P, k, hi);
-        const Phase& f = P.ph[g.ph];
-        const Prob& pb = P.pb[f.prob];
-        const CUtensorMap* mp = maps.m[f.prob];
-        const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
-        const uint32_t bytes = kABytes + uint32_t(f.bn) * kBK * 2;  // per K-block
-        bool t_ready = false;
-        for (int64_t kk = g.s; kk < g.e; ++it) {
-          const int s = int(it % STAGES);
-          const int n = int(g.e - kk < KPS ? g.e - kk : KPS);  // K-blocks in this stage
-          if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitLimitNs)) {
-            *abort_flag = 1;
-            break;
-          }
-          if (!f.down && !t_ready && int(kk + n - 1 - g.tstart) >= f.nkb_base) {
-            // The rows of T this tile reads must be complete before TMA reads them.
-            bool ok = true;
-            if (P.swap) {
-              for (int i = 0; i < pb.down_tiles && ok; ++i)
-                ok = wait_flag(P.flags + pb.flag_base + i, kWaitLimitNs);
-            } else {
-              ok = wait_flag(P.flags + pb.flag_base + ta, kWaitLimitNs);
+      for (int sec = 0; sec < 2 && !*abort_flag; ++sec) {
+        const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
+        for (int64_t k = lo; k < hi && !*abort_flag;) {
+          const Seg g = locate(P, sec, k, hi);
+          const Phase& f = P.ph[g.ph];
+          const Prob& pb = P.pb[f.prob];
+          const CUtensorMap* mp = maps.m[f.prob];
+          const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
+          const uint32_t bytes = kABytes + uint32_t(f.bn) * kBK * 2;
+          const int64_t n = g.e - g.s;
+          bool t_ready = false;
+          for (int64_t i = 0; i < n; ++i, ++it) {
+            const int kl = int(piece_kb(g, f.na, i) - g.tstart);
+            const bool adapter = kl < f.na;
+            if (adapter && !t_ready) {
+              // The rows of T this tile reads must be complete before TMA reads them.
+              bool ok = true;
+              if (P.swap) {
+                for (int j = 0; j < pb.ttiles && ok; ++j)
+                  ok = wait_flag(P.tflag + pb.tflag0 + j, kWaitLimitNs);
+              } else {
+                ok = wait_flag(P.tflag + pb.tflag0 + ta, kWaitLimitNs);
+              }
+              if (!ok) {
+                *abort_flag = 1;
+                break;
+              }
+              fence_proxy_async();
+              t_ready = true;
             }
-            if (!ok) {
+            const int s = int(it % STAGES);
+            if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitLimitNs)) {
               *abort_flag = 1;
               break;
             }
-            fence_proxy_async();
-            t_ready = true;
-          }
-          uint8_t* sa = smem + s * kStage;
-          ptx::mbar_arrive_expect_tx(&full[s], bytes * uint32_t(n));
-          for (int j = 0; j < n; ++j, ++kk) {
-            const int kl = int(kk - g.tstart);
             const CUtensorMap *ma, *mb;
             int kc;
             if (f.down) {
               ma = &mp[P.swap ? MAP_A : MAP_X];
               mb = &mp[P.swap ? MAP_X : MAP_A];
               kc = kl * kBK;
-            } else if (kl < f.nkb_base) {
+            } else if (!adapter) {
               ma = &mp[P.swap ? MAP_W : MAP_X];
               mb = &mp[P.swap ? MAP_X : MAP_W];
-              kc = kl * kBK;
+              kc = (kl - f.na) * kBK;
             } else {
               ma = &mp[P.swap ? MAP_B : MAP_T];
               mb = &mp[P.swap ? MAP_T : MAP_B];
-              kc = (kl - f.nkb_base) * kBK;
+              kc = kl * kBK;
             }
-            ptx::tma_load_2d(sa + j * kABytes, ma, &full[s], kc, ta * kBM, polA);
-            ptx::tma_load_2d(sa + KPS * kABytes + j * kBSub, mb, &full[s], kc, tb * f.bn, polB);
+            uint8_t* sa = smem + s * kStage;
+            ptx::mbar_arrive_expect_tx(&full[s], bytes);
+            ptx::tma_load_2d(sa, ma, &full[s], kc, ta * kBM, polA);
+            ptx::tma_load_2d(sa + kABytes, mb, &full[s], kc, tb * f.bn, polB);
           }
+          k = g.e;
         }
-        k = g.e;
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
@@ -352,167 +481,222 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
           ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kWaitLimitNs);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       uint32_t it = 0;
       int seg = 0;
-      for (int64_t k = lo; k < hi && !*abort_flag; ++seg) {
-        const Seg g = locate(P, k, hi);
-        const Phase& f = P.ph[g.ph];
-        const int acc = seg & 1;
-        if (seg >= 2 && !ptx::mbar_wait(&tempty[acc], ((seg >> 1) - 1) & 1, kWaitLimitNs)) {
-          *abort_flag = 1;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t d = tmem + uint32_t(acc * BNMAX);
-        const uint32_t idesc = ptx::idesc_bf16_f32(kBM, f.bn);
-        for (int64_t kk = g.s; kk < g.e; ++it) {
-          const int s = int(it % STAGES);
-          const int n = int(g.e - kk < KPS ? g.e - kk : KPS);
-          if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, kWaitLimitNs)) {
+      for (int sec = 0; sec < 2 && !*abort_flag; ++sec) {
+        const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
+        for (int64_t k = lo; k < hi && !*abort_flag; ++seg) {
+          const Seg g = locate(P, sec, k, hi);
+          const Phase& f = P.ph[g.ph];
+          const int acc = seg & 1;
+          if (seg >= 2 && !ptx::mbar_wait(&tempty[acc], ((seg >> 1) - 1) & 1, kWaitLimitNs)) {
             *abort_flag = 1;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(smem + s * kStage);
-          const uint32_t sb = sa + KPS * kABytes;
-          for (int j = 0; j < n; ++j, ++kk) {
+          const uint32_t d = tmem + uint32_t(acc * BNMAX);
+          const uint32_t idesc = ptx::idesc_bf16_f32(kBM, f.bn);
+          const int64_t n = g.e - g.s;
+          for (int64_t i = 0; i < n; ++i, ++it) {
+            const int s = int(it % STAGES);
+            if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, kWaitLimitNs)) {
+              *abort_flag = 1;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(smem + s * kStage);
+            const uint32_t sb = sa + kABytes;
 #pragma unroll
             for (int u = 0; u < kBK / kUmmaK; ++u)
-              ptx::umma_f16(d, ptx::sw128_kmajor_desc(sa + j * kABytes + u * 32),
-                            ptx::sw128_kmajor_desc(sb + j * kBSub + u * 32), idesc,
-                            (kk > g.s || u > 0) ? 1u : 0u);
+              ptx::umma_f16(d, ptx::sw128_kmajor_desc(sa + u * 32), ptx::sw128_kmajor_desc(sb + u * 32),
+                            idesc, (i > 0 || u > 0) ? 1u : 0u);
+            ptx::umma_commit(&empty[s]);
           }
-          ptx::umma_commit(&empty[s]);
+          ptx::umma_commit(&tfull[acc]);
+          k = g.e;
         }
-        ptx::umma_commit(&tfull[acc]);
-        k = g.e;
       }
       // once this arrives, every MMA issued by this thread has completed
       ptx::umma_commit(mma_done);
       ptx::mbar_wait(mma_done, 0, kWaitLimitNs);
     }
+    __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;
     const int et = threadIdx.x - 64;
+    uint32_t stg_phase = 0;  // phases of stg_bar used so far
     int seg = 0;
-    for (int64_t k = lo; k < hi; ++seg) {
-      const Seg g = locate(P, k, hi);
-      const Phase& f = P.ph[g.ph];
-      const Prob& pb = P.pb[f.prob];
-      const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
-      const int acc = seg & 1;
-      if (!ptx::mbar_wait(&tfull[acc], (seg >> 1) & 1, kWaitLimitNs)) *abort_flag = 1;
-      epi_sync();
-      if (*abort_flag) break;
-      ptx::tc_fence_after();
-      const uint32_t tq = tmem + uint32_t(acc * BNMAX) + (uint32_t(q * 32) << 16);
-      const bool whole = (g.s == g.tstart && g.e == g.tend);
-      bool finish = whole;
-      if (whole) {
-        for (int c = 0; c < f.bn; c += 16) {
-          uint32_t r[16];
-          ptx::tmem_ld_32x32b_x16(tq + c, r);
-          ptx::tmem_ld_wait(r);
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          store16(P, f, pb, ta, tb, row, c, v);
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
-      } else {
-        // Part of a tile: leave a partial; the last CTA of the tile to arrive
-        // adds the partials in CTA order and writes the result.
-        const int slot = (g.s == lo) ? 0 : 1;
-        // partial layout [column/4][row][4]: each thread moves float4s and a
-        // warp touches 512 contiguous bytes per access
-        float4* dst = reinterpret_cast<float4*>(
-            P.partial + (size_t(blockIdx.x) * 2 + slot) * (size_t(P.bnmax) * kBM));
-        for (int c = 0; c < f.bn; c += 16) {
-          uint32_t r[16];
-          ptx::tmem_ld_32x32b_x16(tq + c, r);
-          ptx::tmem_ld_wait(r);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            __stcg(dst + ((c >> 2) + i) * kBM + row,
-                   make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                               __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
-        __threadfence();
-        epi_sync();
-        const int c0 = cta_of(g.tstart, G, P.total);
-        const int c1 = cta_of(g.tend - 1, G, P.total);
-        if (et == 0) *last_flag = atomicAdd(P.counters + c0, 1) == c1 - c0;
-        epi_sync();
-        finish = *last_flag != 0;
-        if (finish) {
-          __threadfence();
-          // Sum the partials in CTA order: 32 columns of up to 4 CTAs in flight.
-          for (int c = 0; c < f.bn; c += 32) {
-            float4 sum[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cb = c0; cb <= c1; cb += 4) {
-              float4 t[4][8];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int cc = cb + u;
-                const float4* src = nullptr;
-                if (cc <= c1) {
-                  const int sl = range_lo(cc, G, P.total) >= g.tstart ? 0 : 1;
-                  src = reinterpret_cast<const float4*>(
-                      P.partial + (size_t(cc) * 2 + sl) * (size_t(P.bnmax) * kBM));
+    for (int sec = 0; sec < 2; ++sec) {
+      const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
+      for (int64_t k = lo; k < hi; ++seg) {
+        const Seg g = locate(P, sec, k, hi);
+        const Phase& f = P.ph[g.ph];
+        const Prob& pb = P.pb[f.prob];
+        const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
+        const int acc = seg & 1;
+        const bool whole = g.s == g.tstart && g.e == g.tend;
+        const bool finisher = !whole && g.s == g.tstart;
+        const int c1 = finisher ? owner_of(P, sec, g.tend - 1) : cta;
+        float pre[kPreMerge ? BNMAX : 1];
+        bool fail = false;
+        if (finisher) {
+          if constexpr (kPreMerge) {
+            // While the tensor cores finish this piece, bring the contributors'
+            // partials into shared memory (one bulk copy each, issued as soon as
+            // its flag is up) and sum them in CTA order.
+            const uint32_t bytes = uint32_t(f.bn) * kBM * 4;
+            bool any = false;
+            int c = cta + 1;
+            while (c <= c1) {
+              int nb = 0, cs = c;
+              for (; cs <= c1 && nb < kSlots; ++cs) nb += P.lo[sec][cs] < P.lo[sec][cs + 1];
+              if (nb == 0) break;
+              if (et == 0) {
+                // first batch: wait for every contributor at once (they finish together)
+                if (c == cta + 1) fail = !wait_ready(P, sec, cta + 1, c1, kWaitLimitNs);
+                fence_proxy_async();
+                ptx::mbar_arrive_expect_tx(stg_bar, fail ? 0u : bytes * uint32_t(nb));
+                int i = 0;
+                for (int cc = c; cc < cs && !fail; ++cc) {
+                  if (P.lo[sec][cc] == P.lo[sec][cc + 1]) continue;
+                  ptx::bulk_load(staging + size_t(i) * BNMAX * kBM,
+                                 P.partial + (size_t(cc) * 2 + sec) * kSlot, bytes, stg_bar);
+                  ++i;
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  t[u][i] = (src && c + 4 * i < f.bn) ? __ldcg(src + ((c >> 2) + i) * kBM + row)
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
               }
+              if (!ptx::mbar_wait(stg_bar, stg_phase & 1, kWaitLimitNs)) fail = true;
+              ++stg_phase;
+              if (!fail) {
+                const float4* st4 = reinterpret_cast<const float4*>(staging);
+                for (int i = 0; i < nb; ++i) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  sum[i].x += t[u][i].x;
-                  sum[i].y += t[u][i].y;
-                  sum[i].z += t[u][i].z;
-                  sum[i].w += t[u][i].w;
+                  for (int j = 0; j < BNMAX / 4; ++j) {
+                    if (4 * j < f.bn) {
+                      const float4 t = st4[(size_t(i) * BNMAX / 4 + j) * kBM + row];
+                      pre[4 * j] = any ? pre[4 * j] + t.x : t.x;
+                      pre[4 * j + 1] = any ? pre[4 * j + 1] + t.y : t.y;
+                      pre[4 * j + 2] = any ? pre[4 * j + 2] + t.z : t.z;
+                      pre[4 * j + 3] = any ? pre[4 * j + 3] + t.w : t.w;
+                    }
+                  }
+                  any = true;
                 }
+              }
+              // every thread is done with the slots before they are refilled
+              fail = epi_sync_or(fail);
+              if (fail) break;
+              c = cs;
             }
+            if (!any) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (c + 16 * h >= f.bn) break;
+              for (int j = 0; j < (kPreMerge ? BNMAX : 1); ++j) pre[j] = 0.f;
+            }
+          } else {
+            // The contributors left their pieces as the first piece of their
+            // ranges; their flags are normally up long before this point.
+            fail = !wait_ready(P, sec, cta + 1, c1, kWaitLimitNs);
+          }
+        }
+        if (!ptx::mbar_wait(&tfull[acc], (seg >> 1) & 1, kWaitLimitNs)) fail = true;
+        if (epi_sync_or(fail || *abort_flag)) {
+          *abort_flag = 1;
+          goto done;
+        }
+        ptx::tc_fence_after();
+        {
+          const uint32_t tq = tmem + uint32_t(acc * BNMAX) + (uint32_t(q * 32) << 16);
+          if (whole) {
+            for (int c0 = 0; c0 < f.bn; c0 += 16) {
               float v[16];
+              tmem_ld16f(tq + c0, v);
+              store16(P, f, pb, ta, tb, row, c0, v);
+            }
+          } else if (!finisher) {
+            // contributor: leave the piece as a partial and raise this CTA's flag
+            float4* dst = reinterpret_cast<float4*>(P.partial + (size_t(cta) * 2 + sec) * kSlot);
+            for (int c0 = 0; c0 < f.bn; c0 += 16) {
+              float v[16];
+              tmem_ld16f(tq + c0, v);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                v[4 * i] = sum[4 * h + i].x;
-                v[4 * i + 1] = sum[4 * h + i].y;
-                v[4 * i + 2] = sum[4 * h + i].z;
-                v[4 * i + 3] = sum[4 * h + i].w;
+              for (int i = 0; i < 4; ++i)
+                __stcg(dst + ((c0 >> 2) + i) * kBM + row,
+                       make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            }
+          } else if constexpr (kPreMerge) {
+#pragma unroll
+            for (int c0 = 0; c0 < BNMAX; c0 += 16) {
+              if (c0 < f.bn) {
+                float v[16];
+                tmem_ld16f(tq + c0, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += pre[c0 + j];
+                store16(P, f, pb, ta, tb, row, c0, v);
               }
-              store16(P, f, pb, ta, tb, row, c + 16 * h, v);
+            }
+          } else {
+            // finisher of a wide tile: own accumulator, then the partials of
+            // up to four contributors at a time, in CTA order
+            for (int c0 = 0; c0 < f.bn; c0 += 16) {
+              float v[16];
+              tmem_ld16f(tq + c0, v);
+              for (int cb = cta + 1; cb <= c1; cb += 4) {
+                float4 t[4][4];
+                bool use[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int c = cb + u;
+                  use[u] = c <= c1 && P.lo[sec][c] < P.lo[sec][c + 1];
+                  const float4* src = reinterpret_cast<const float4*>(
+                      P.partial + (size_t(use[u] ? c : cta) * 2 + sec) * kSlot);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    t[u][i] = use[u] ? __ldcg(src + ((c0 >> 2) + i) * kBM + row)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (use[u]) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      v[4 * i] += t[u][i].x;
+                      v[4 * i + 1] += t[u][i].y;
+                      v[4 * i + 2] += t[u][i].z;
+                      v[4 * i + 3] += t[u][i].w;
+                    }
+                  }
+              }
+              store16(P, f, pb, ta, tb, row, c0, v);
             }
           }
-          if (et == 0) P.counters[c0] = 0;
+          // the accumulator may be reused
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+          // A partial (read by the finisher's bulk copies) or a finished T tile
+          // (read by TMA in other CTAs) is published with a release: every
+          // thread orders its stores before the async proxy, the barrier
+          // orders them before thread 0, whose fence and flag store release them.
+          const bool publish_partial = !whole && !finisher;
+          const bool publish_t = f.down && (whole || finisher);
+          if (publish_partial || publish_t) {
+            fence_proxy_async();
+            epi_sync();
+            if (et == 0) {
+              fence_acq_rel_gpu();
+              st_release(publish_partial ? P.ready + sec * P.grid + cta : P.tflag + pb.tflag0 + ta, 1);
+            }
+          }
         }
+        k = g.e;
       }
-      if (f.down && finish) {
-        // publish this down tile: its part of T is in global memory
-        fence_proxy_async();
-        __threadfence();
-        epi_sync();
-        if (et == 0) st_release(P.flags + pb.flag_base + ta, 1);
-      }
-      k = g.e;
     }
+  done:;
   }
 
   ptx::tc_fence_before();
@@ -567,14 +751,15 @@ int pick_bn(int64_t n) {
 
 struct Layout {
   Params P;
+  int tflags;
   size_t off_t[kMaxLoraProblems];
   size_t off_partial, off_sync, sync_bytes;
   size_t off_cast[kMaxLoraProblems][4];  // fp32 mode: bf16 copies of x, W, A, B
   size_t bytes;
 };
 
-// Host-side schedule: phases of the global K-block sequence, grid size and
-// workspace layout.  Depends only on shapes and the SM count.
+// Host-side schedule: the phases of both sections, the grid, each CTA's
+// ranges and the workspace layout.  Depends only on shapes and the SM count.
 bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms, Layout& L) {
   if (n < 1 || n > kMaxLoraProblems) return false;
   std::memset(&L, 0, sizeof(L));
@@ -583,40 +768,43 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   P.swap = M <= 256 ? 1 : 0;
   P.out_f32 = dtype == UNO_F32;
   const int bn_tok = pick_bn(M);
+  int nph = 0, tflags = 0, bnmax = 16, max_down_nkb = 0;
   int64_t kb = 0;
-  int nph = 0, flags = 0, bnmax = 16;
-  for (int p = 0; p < n; ++p) {  // down-projection phases first
+  P.ph0[kDown] = 0;
+  for (int p = 0; p < n; ++p) {  // down section: T tiles of every adapted problem
     Prob& b = P.pb[p];
     b.d_out = int(pr[p].d_out);
     b.r = int(pr[p].rank);
     b.scale = pr[p].rank > 0 ? pr[p].alpha / float(pr[p].rank) : 0.f;
-    b.flag_base = flags;
+    b.tflag0 = tflags;
     if (pr[p].rank == 0) continue;
     Phase& f = P.ph[nph++];
     f.kb_start = kb;
     f.prob = p;
     f.down = 1;
-    f.nkb = f.nkb_base = int((pr[p].d_in + kBK - 1) / kBK);
-    if (P.swap) {
-      f.tiles_a = int((pr[p].rank + kBM - 1) / kBM);
-      f.bn = bn_tok;
-    } else {
-      f.tiles_a = int((M + kBM - 1) / kBM);
-      f.bn = pick_bn(pr[p].rank);
-    }
+    f.na = 0;
+    f.nkb = int((pr[p].d_in + kBK - 1) / kBK);
+    // one tile along N: bn covers every token (swap) or the whole rank
+    f.tiles_a = int(((P.swap ? pr[p].rank : M) + kBM - 1) / kBM);
+    f.bn = P.swap ? bn_tok : pick_bn(pr[p].rank);
     f.tiles = f.tiles_a;
-    b.down_tiles = f.tiles;
-    flags += f.tiles;
+    b.ttiles = f.tiles;
+    tflags += f.tiles;
     kb += int64_t(f.tiles) * f.nkb;
     bnmax = std::max(bnmax, f.bn);
+    max_down_nkb = std::max(max_down_nkb, f.nkb);
   }
-  for (int p = 0; p < n; ++p) {  // then the main phases
+  P.ph1[kDown] = nph;
+  const int64_t D = kb;
+  P.ph0[kMain] = nph;
+  kb = 0;
+  for (int p = 0; p < n; ++p) {  // main section: y tiles
     Phase& f = P.ph[nph++];
     f.kb_start = kb;
     f.prob = p;
     f.down = 0;
-    f.nkb_base = int((pr[p].d_in + kBK - 1) / kBK);
-    f.nkb = f.nkb_base + int((pr[p].rank + kBK - 1) / kBK);
+    f.na = int((pr[p].rank + kBK - 1) / kBK);
+    f.nkb = f.na + int((pr[p].d_in + kBK - 1) / kBK);
     if (P.swap) {
       f.tiles_a = int((pr[p].d_out + kBM - 1) / kBM);
       f.bn = bn_tok;
@@ -629,20 +817,40 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     kb += int64_t(f.tiles) * f.nkb;
     bnmax = std::max(bnmax, f.bn);
   }
-  P.nph = nph;
-  P.total = kb;
+  P.ph1[kMain] = nph;
+  const int64_t Mn = kb, Wt = D + Mn;
   P.bnmax = bnmax;
+  L.tflags = tflags;
   // One CTA per SM, at least 4 K-blocks each.
-  P.grid = int(std::max<int64_t>(1, std::min<int64_t>(sms, kb / 4)));
+  const int G = int(std::max<int64_t>(1, std::min<int64_t>(std::min(sms, kMaxGrid), Wt / 4)));
+  P.grid = G;
+  // Down section: a few K-blocks per CTA so that T is complete early, but a
+  // T tile in at most 16 pieces (a long d_in takes longer pieces); at large
+  // M, where T tiles are many and cheap, whole tiles up to half a CTA's share.
+  int Gd = 0;
+  if (D > 0) {
+    int64_t kd = std::max<int64_t>(4, (max_down_nkb + 15) / 16);
+    if (!P.swap) kd = std::max<int64_t>(kd, std::min<int64_t>(max_down_nkb, Wt / G / 2));
+    Gd = int(std::max<int64_t>(1, std::min<int64_t>(G, (D + kd - 1) / kd)));
+  }
+  for (int c = 0; c <= G; ++c) P.lo[kDown][c] = c <= Gd && Gd > 0 ? int64_t(c) * D / Gd : D;
+  // Main section: CTA c's range ends where the first c+1 CTAs have streamed
+  // (c+1)/G of all K-blocks, down ones included.
+  P.lo[kMain][0] = 0;
+  for (int c = 1; c < G; ++c) {
+    const int64_t v = int64_t(c) * Wt / G - P.lo[kDown][c];
+    P.lo[kMain][c] = std::min(Mn, std::max(P.lo[kMain][c - 1], v));
+  }
+  P.lo[kMain][G] = Mn;
   size_t o = 0;
   for (int p = 0; p < n; ++p) {
     L.off_t[p] = o;
     o = align_up(o + size_t(M) * size_t(pr[p].rank) * 2, 256);
   }
   L.off_partial = o;
-  o = align_up(o + size_t(P.grid) * 2 * size_t(bnmax) * kBM * sizeof(float), 256);
+  o = align_up(o + size_t(G) * 2 * size_t(bnmax) * kBM * sizeof(float), 256);
   L.off_sync = o;
-  L.sync_bytes = align_up((size_t(P.grid) + size_t(flags)) * sizeof(int), 256);
+  L.sync_bytes = align_up((2 * size_t(G) + size_t(tflags)) * sizeof(int), 256);
   o += L.sync_bytes;
   if (dtype == UNO_F32) {
     for (int p = 0; p < n; ++p) {
@@ -668,29 +876,28 @@ cudaError_t cast_to_bf16(const void* in, void* out, int64_t n, cudaStream_t st) 
 
 template <int BNMAX>
 cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
-  constexpr int KPS = kps_for<BNMAX>();
   static std::once_flag once[64];
   static cudaError_t attr_err[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   dev &= 63;
   std::call_once(once[dev], [&] {
-    attr_err[dev] = cudaFuncSetAttribute(grouped_lora_gemm_kernel<BNMAX, KPS>,
+    attr_err[dev] = cudaFuncSetAttribute(grouped_lora_gemm_kernel<BNMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem_bytes_for<BNMAX, KPS>()));
+                                         int(smem_bytes_for<BNMAX>()));
   });
   if (attr_err[dev] != cudaSuccess) return attr_err[dev];
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(P.grid));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes_for<BNMAX, KPS>();
+  cfg.dynamicSmemBytes = smem_bytes_for<BNMAX>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX, KPS>, maps, P);
+  return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX>, maps, P);
 }
 
 }  // namespace
@@ -710,8 +917,8 @@ int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, v
   char* w = static_cast<char*>(ws);
   Params& P = L.P;
   P.partial = reinterpret_cast<float*>(w + L.off_partial);
-  P.counters = reinterpret_cast<int*>(w + L.off_sync);
-  P.flags = P.counters + P.grid;
+  P.ready = reinterpret_cast<int*>(w + L.off_sync);
+  P.tflag = P.ready + 2 * P.grid;
   Maps maps;
   std::memset(&maps, 0, sizeof(maps));
   for (int p = 0; p < n; ++p) {
@@ -735,7 +942,7 @@ int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, v
     b.t = w + L.off_t[p];
     b.gate = q.gate;
     int bn_main = 0, bn_down = 0;
-    for (int i = 0; i < P.nph; ++i)
+    for (int i = 0; i < P.ph1[kMain]; ++i)
       if (P.ph[i].prob == p) (P.ph[i].down ? bn_down : bn_main) = P.ph[i].bn;
     CUtensorMap* m = maps.m[p];
     const bool sw = P.swap != 0;
