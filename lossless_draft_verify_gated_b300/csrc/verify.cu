@@ -80,9 +80,10 @@ __device__ __forceinline__ const float* row_ptr(const float* p, const float* q, 
 }
 
 __global__ void __launch_bounds__(kThreads)
-verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int64_t K,
-                    int64_t Kp, int64_t V, int splits, int64_t chunk, float2* __restrict__ part,
-                    int* __restrict__ counter) {
+verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                    const int32_t* __restrict__ draft, int64_t K, int64_t Kp, int64_t V,
+                    int splits, int64_t chunk, float2* __restrict__ part,
+                    float* __restrict__ gathered, int* __restrict__ counter) {
   const int64_t unit = blockIdx.x;
   const int64_t row = unit / splits;
   const int split = int(unit - row * splits);
@@ -90,6 +91,10 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, in
   const int64_t b = row / per_seq;
   const int64_t j = row - b * per_seq;
   if (j == 0 && split == 0 && threadIdx.x == 0) counter[b] = 0;  // finish kernel's arrival count
+  // The drafted token of this row's position (AR row j or draft row j - Kp);
+  // the thread that streams its logit keeps it for the acceptance test.
+  const int64_t pos = j < Kp ? j : j - Kp;
+  const int64_t xd = pos < K ? int64_t(draft[b * K + pos]) : -1;
 
   const float* r = row_ptr(p, q, b, j, K, Kp, V);
   const int64_t v0 = int64_t(split) * chunk;
@@ -104,18 +109,35 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, in
 
   MS acc{-INFINITY, 0.f};
   const int tid = threadIdx.x;
-  if (tid < va - v0) ms_add1(acc, r[v0 + tid]);
-  if (tid < v1 - vb) ms_add1(acc, r[vb + tid]);
+  if (tid < va - v0) {
+    const float x = r[v0 + tid];
+    ms_add1(acc, x);
+    if (v0 + tid == xd) gathered[row] = x;
+  }
+  if (tid < v1 - vb) {
+    const float x = r[vb + tid];
+    ms_add1(acc, x);
+    if (vb + tid == xd) gathered[row] = x;
+  }
   const float4* vp = reinterpret_cast<const float4*>(r + va);
-  for (int64_t i = tid; i < nvec; i += int64_t(kThreads) * kUnroll) {
+  // chunks hold < 2^31 elements: 32-bit indices in the streaming loop
+  const int nv = int(nvec);
+  const int xq = (xd >= va && xd < vb) ? int((xd - va) >> 2) : -1;  // float4 holding the drafted token
+  for (int i = tid; i < nv; i += kThreads * kUnroll) {
     float4 t[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t idx = i + int64_t(u) * kThreads;
-      t[u] = idx < nvec ? __ldcs(vp + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      const int idx = i + u * kThreads;
+      t[u] = idx < nv ? __ldcs(vp + idx) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) ms_add4(acc, t[u].x, t[u].y, t[u].z, t[u].w);
+    for (int u = 0; u < kUnroll; ++u) {
+      ms_add4(acc, t[u].x, t[u].y, t[u].z, t[u].w);
+      if (xq == i + u * kThreads) {
+        const int c = int((xd - va) & 3);
+        gathered[row] = c == 0 ? t[u].x : c == 1 ? t[u].y : c == 2 ? t[u].z : t[u].w;
+      }
+    }
   }
 
   acc = warp_merge(acc);
@@ -162,7 +184,8 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
                      const int32_t* __restrict__ draft, const float* __restrict__ u_acc,
                      const float* __restrict__ u_res, int64_t K, int64_t Kp, int64_t V,
                      int splits, int race_splits, int64_t race_chunk,
-                     const float2* __restrict__ part, RacePart* __restrict__ rpart,
+                     const float2* __restrict__ part, const float* __restrict__ gathered,
+                     RacePart* __restrict__ rpart,
                      int* __restrict__ counter, int32_t* __restrict__ n_acc,
                      int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_emit,
                      int32_t* __restrict__ status) {
@@ -244,13 +267,13 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   if (tid == 0) s_n = int(K);
   __syncthreads();
   for (int64_t i = tid; i < K; i += kThreads) {
-    const int32_t x = draft[b * K + i];
-    const float lq = q[(b * K + i) * V + x];
+    // logits of the drafted token, gathered by the statistics pass
+    const float lq = gathered[b * per_seq + Kp + i];
     bool accept;
     if (lq == -INFINITY) {
       accept = true;  // q_i(x) = 0: ratio +inf
     } else {
-      const float lp = p[(b * Kp + i) * V + x];
+      const float lp = gathered[b * per_seq + i];
       const float lr = (lp - s_lz[i]) - (lq - s_lz[Kp + i]);
       const float thr = fminf(1.0f, expf(lr));
       accept = u_acc[b * K + i] < thr;
@@ -285,7 +308,12 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const float* ub = u_res + b * V;
   const int64_t v0 = int64_t(split) * race_chunk;
   const int64_t v1 = min(V, v0 + race_chunk);
-  Cand cr{0.f, -1}, cp{-1.f, -1};
+  // Each thread keeps its best score as a fraction num/den and compares by
+  // cross-multiplication (den = -ln u > 0), dividing once at the end;
+  // probabilities come from exp2 of the scaled, max-shifted logit.
+  constexpr float kLog2e = 1.4426950408889634f;
+  float pn = -1.f, pd = 1.f, rn = 0.f, rd = 1.f;
+  int pvid = -1, rvid = -1;
   constexpr int kRaceUnroll = 4;
   for (int64_t v = v0 + tid; v < v1; v += int64_t(kThreads) * kRaceUnroll) {
     float uu[kRaceUnroll], lp[kRaceUnroll], lq[kRaceUnroll];
@@ -302,14 +330,23 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       const int64_t vi = v + int64_t(i) * kThreads;
       if (vi >= v1) break;
       const float e = -logf(uu[i]);
-      const float pv = expf(lp[i] - mp) * izp;
-      cp = cand_best(cp, Cand{pv / e, int(vi)});
+      const float pv = exp2f((lp[i] - mp) * kLog2e) * izp;
+      if (pv * pd > pn * e) {  // pv / e > pn / pd; ties keep the lower id
+        pn = pv;
+        pd = e;
+        pvid = int(vi);
+      }
       if (residual) {
-        const float rv = pv - expf(lq[i] - mq) * izq;
-        if (rv > 0.f) cr = cand_best(cr, Cand{rv / e, int(vi)});
+        const float rv = pv - exp2f((lq[i] - mq) * kLog2e) * izq;
+        if (rv > 0.f && rv * rd > rn * e) {
+          rn = rv;
+          rd = e;
+          rvid = int(vi);
+        }
       }
     }
   }
+  Cand cr{rvid >= 0 ? rn / rd : 0.f, rvid}, cp{pvid >= 0 ? pn / pd : -1.f, pvid};
   cr = warp_best(cr);
   cp = warp_best(cp);
   if ((tid & 31) == 0) {
@@ -416,11 +453,11 @@ draft_sample_kernel(const float* __restrict__ logits, const float* __restrict__ 
 VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   VerifyPlan pl{};
   pl.rows = Bn * (Kp + K);
-  // Statistics pass: about 8 CTAs of 256 threads per SM in flight; split
-  // rows only while each chunk keeps at least 2048 logits.
-  const int64_t target = int64_t(sms) * 8;
+  // Statistics pass: about 4 CTAs of 256 threads per SM; split rows only
+  // while each chunk keeps at least 4096 logits.
+  const int64_t target = int64_t(sms) * 4;
   int64_t s = pl.rows > 0 ? (target + pl.rows - 1) / pl.rows : 1;
-  s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 2047) / 2048));
+  s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 4095) / 4096));
   int64_t chunk = (V + s - 1) / s;
   chunk = (chunk + 3) & ~int64_t(3);
   pl.chunk = chunk;
@@ -432,7 +469,8 @@ VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   pl.race_chunk = (V + s2 - 1) / s2;
   pl.race_splits = int((V + pl.race_chunk - 1) / pl.race_chunk);
   pl.off_stats = 0;
-  pl.off_race = align_up(pl.off_stats + size_t(pl.rows) * pl.splits * sizeof(float2), 256);
+  pl.off_gather = align_up(pl.off_stats + size_t(pl.rows) * pl.splits * sizeof(float2), 256);
+  pl.off_race = align_up(pl.off_gather + size_t(pl.rows) * sizeof(float), 256);
   pl.off_count = align_up(pl.off_race + size_t(Bn) * pl.race_splits * sizeof(RacePart), 256);
   pl.bytes = align_up(pl.off_count + size_t(Bn) * sizeof(int), 256);
   return pl;
@@ -445,17 +483,18 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                           cudaStream_t st) {
   char* w = static_cast<char*>(ws);
   float2* part = reinterpret_cast<float2*>(w + pl.off_stats);
+  float* gathered = reinterpret_cast<float*>(w + pl.off_gather);
   RacePart* rpart = reinterpret_cast<RacePart*>(w + pl.off_race);
   int* counter = reinterpret_cast<int*>(w + pl.off_count);
   const int64_t g1 = pl.rows * pl.splits;
-  verify_stats_kernel<<<dim3(unsigned(g1)), kThreads, 0, st>>>(p, q, K, Kp, V, pl.splits,
-                                                                pl.chunk, part, counter);
+  verify_stats_kernel<<<dim3(unsigned(g1)), kThreads, 0, st>>>(p, q, draft, K, Kp, V, pl.splits,
+                                                                pl.chunk, part, gathered, counter);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t g2 = Bn * pl.race_splits;
   verify_finish_kernel<<<dim3(unsigned(g2)), kThreads, 0, st>>>(
       p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, part,
-      rpart, counter, n_acc, out_tokens, n_emit, status);
+      gathered, rpart, counter, n_acc, out_tokens, n_emit, status);
   return cudaGetLastError();
 }
 
