@@ -40,6 +40,12 @@
 // (tcgen05.ld) and store y, T or partials, overlapping the next piece's MMAs.
 // Decode-sized M (<= 256 token rows) swaps the operands so that the weights
 // fill the 128-row MMA side and the tokens are N.
+// Launches are chained with programmatic dependent launch: each CTA lets the
+// next launch in the stream start at once, and waits (griddepcontrol.wait)
+// for the previous one before it touches global memory, except for L2
+// prefetch hints of its first weight tiles (L2 is the coherence point, so a
+// hint can never return stale data).  A one-CTA kernel before each launch
+// clears the schedule's flags once the previous launch has finished.
 // Every wait is bounded (2 s): a timeout sets the device error word and the
 // CTA unwinds.
 #include <cuda.h>
@@ -62,11 +68,13 @@ namespace {
 constexpr int kBM = 128;    // MMA M: A-operand rows per tile (= TMEM lanes)
 constexpr int kBK = 64;     // K elements per K-block (one 128-byte swizzle row of bf16)
 constexpr int kUmmaK = 16;  // K of one tcgen05.mma for 16-bit inputs
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;  // warps: 0 TMA, 1 MMA, 2-5 epilogue
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 2 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
+constexpr int kPrefetchKBlocks = 24;
+constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;  // weight tiles hinted into L2 before the previous launch ends
 constexpr int kDown = 0, kMain = 1;
 
 enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, kMapsPerProblem = 5 };
@@ -81,7 +89,8 @@ struct Phase {
   int tiles;
   int tiles_a;       // tiles along the A-operand rows (tile = tb * tiles_a + ta)
   int nkb;           // K-blocks per tile
-  int na;            // of which adapter K-blocks, first in the flat order (0 in the down section)
+  int na;            // of which adapter K-blocks, first in the flat order (large-M path)
+  int nad;           // adapter K-blocks appended to every piece (swap path)
   int prob;
   int down;          // 1: T = gate*scale*x.A^T;  0: y = T.B^T + x.W^T
   int bn;            // MMA N (B-operand rows per tile)
@@ -103,6 +112,7 @@ struct Params {
   Prob pb[kMaxLoraProblems];
   int ph0[2], ph1[2];  // section s holds phases [ph0[s], ph1[s])
   int swap;
+  int localt;  // swap path with per-piece adapter
   int M;
   int out_f32;
   int grid;
@@ -113,41 +123,67 @@ struct Params {
   int* tflag;      // [T tiles]: the rows of T of the tile are written
 };
 
-// Shared memory: a ring of one K-block per stage (A sub-tile, then B
-// sub-tile) and, for decode-sized tiles (N <= 64), a staging area into which a
-// finisher bulk-copies its contributors' partials.
+// Shared memory (per CTA): a ring of STAGES stages, each one K-block of the
+// A operand (128 x 64), the B operand (BNMAX x 64) and, when each piece
+// computes its own share of the adapter (LOCALT), a 128 x 64 slice of the
+// down matrix; with LOCALT, the piece's adapter input T' as the B operand of
+// its up-projection (two 64-wide K-blocks); then, for decode-sized tiles
+// (N <= 64), a staging area into which a finisher bulk-copies its
+// contributors' partials.
 constexpr int kMaxStages = 10;
-constexpr uint32_t kStagingBytes = 96 * 1024;
+constexpr uint32_t kABytes = kBM * kBK * 2;  // one 128 x 64 bf16 sub-tile
+constexpr int kMaxLocalRank = 128;           // LOCALT keeps T' for ranks <= 128
 
 template <int BNMAX>
 __host__ __device__ constexpr bool pre_merge() {
   return BNMAX <= 64;
 }
-template <int BNMAX>
+template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t staging_bytes() {
-  return pre_merge<BNMAX>() ? kStagingBytes : 0;
+  return pre_merge<BNMAX>() ? (LOCALT ? 32u : 96u) * 1024 : 0u;
 }
-template <int BNMAX>
+template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr int staging_slots() {  // partials the staging area holds at once
-  return pre_merge<BNMAX>() ? int(kStagingBytes / (uint32_t(BNMAX) * 128 * 4)) : 0;
+  return pre_merge<BNMAX>() ? int(staging_bytes<BNMAX, LOCALT>() / (uint32_t(BNMAX) * 128 * 4)) : 0;
 }
-template <int BNMAX>
+template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t stage_bytes() {
-  return uint32_t(kBM * kBK * 2 + BNMAX * kBK * 2);
+  return kABytes + uint32_t(BNMAX) * kBK * 2 + (LOCALT ? kABytes : 0u);
 }
-template <int BNMAX>
+template <int BNMAX, bool LOCALT>
+__host__ __device__ constexpr uint32_t tprime_bytes() {
+  return LOCALT ? uint32_t(BNMAX) * 128u * uint32_t(kMaxLocalRank / kBK) : 0u;
+}
+template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr int stages_for() {
-  return int((220 * 1024 - staging_bytes<BNMAX>()) / stage_bytes<BNMAX>()) < kMaxStages
-             ? int((220 * 1024 - staging_bytes<BNMAX>()) / stage_bytes<BNMAX>())
+  return int((216 * 1024 - staging_bytes<BNMAX, LOCALT>() - tprime_bytes<BNMAX, LOCALT>()) /
+             stage_bytes<BNMAX, LOCALT>()) < kMaxStages
+             ? int((216 * 1024 - staging_bytes<BNMAX, LOCALT>() - tprime_bytes<BNMAX, LOCALT>()) /
+                   stage_bytes<BNMAX, LOCALT>())
              : kMaxStages;
 }
+// TMEM accumulators: y (double-buffered when TMEM allows) and, with LOCALT,
+// the piece's T.
+template <int BNMAX, bool LOCALT>
+__host__ __device__ constexpr int acc_bufs() {
+  return (LOCALT && 3 * BNMAX > 512) ? 1 : 2;
+}
+template <int BNMAX, bool LOCALT>
+__host__ __device__ constexpr uint32_t tmem_cols() {
+  return (acc_bufs<BNMAX, LOCALT>() + (LOCALT ? 1 : 0)) * BNMAX <= 32    ? 32u
+         : (acc_bufs<BNMAX, LOCALT>() + (LOCALT ? 1 : 0)) * BNMAX <= 64  ? 64u
+         : (acc_bufs<BNMAX, LOCALT>() + (LOCALT ? 1 : 0)) * BNMAX <= 128 ? 128u
+         : (acc_bufs<BNMAX, LOCALT>() + (LOCALT ? 1 : 0)) * BNMAX <= 256 ? 256u
+                                                                         : 512u;
+}
 // Barriers and the TMEM slot, then a copy of the kernel parameters.
-constexpr uint32_t kBarrierBytes = 256;
+constexpr uint32_t kBarrierBytes = 512;
 constexpr uint32_t kParamsBytes = (uint32_t(sizeof(Params)) + 15u) & ~15u;
-template <int BNMAX>
+template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t smem_bytes_for() {
-  return uint32_t(stages_for<BNMAX>()) * stage_bytes<BNMAX>() + staging_bytes<BNMAX>() + kBarrierBytes +
-         kParamsBytes + 1024;
+  return uint32_t(stages_for<BNMAX, LOCALT>()) * stage_bytes<BNMAX, LOCALT>() +
+         tprime_bytes<BNMAX, LOCALT>() + staging_bytes<BNMAX, LOCALT>() + kBarrierBytes + kParamsBytes +
+         1024;
 }
 
 struct Seg {
@@ -344,30 +380,40 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-template <int BNMAX>
+// SWAP: decode-sized M, the weights are the A operand (128 rows of W per
+// tile) and the tokens are N.  LOCALT (swap only): every piece computes its
+// own share of T = x.A^T and applies it; otherwise T is computed once per
+// T tile in the down section and read back by TMA.
+template <int BNMAX, bool SWAP, bool LOCALT>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params Pk) {
-  constexpr int STAGES = stages_for<BNMAX>();
-  constexpr uint32_t kABytes = kBM * kBK * 2;       // A sub-tile (128 x 64)
-  constexpr uint32_t kStage = stage_bytes<BNMAX>();  // A sub-tile, then the B slot
-  constexpr uint32_t kTmemCols = 2 * BNMAX < 32 ? 32 : 2 * BNMAX;
-  constexpr size_t kSlot = size_t(BNMAX) * kBM;      // floats of one partial slot
-  // Decode-sized tiles: a finisher sums its contributors' partials into
-  // registers while its own last piece is still in the tensor cores.
+  static_assert(SWAP || !LOCALT, "per-piece adapter needs the swapped operands");
+  constexpr int STAGES = stages_for<BNMAX, LOCALT>();
+  constexpr uint32_t kStage = stage_bytes<BNMAX, LOCALT>();  // A sub-tile, B slot, (LOCALT) down slice
+  constexpr uint32_t kBSlot = uint32_t(BNMAX) * kBK * 2;
+  constexpr uint32_t kTmemCols = tmem_cols<BNMAX, LOCALT>();
+  constexpr int kAcc = acc_bufs<BNMAX, LOCALT>();
+  constexpr size_t kSlot = size_t(BNMAX) * kBM;  // floats of one partial slot
+  // Decode-sized tiles: a finisher sums its contributors' partials while its
+  // own last piece is still in the tensor cores.
   constexpr bool kPreMerge = pre_merge<BNMAX>();
-  constexpr int kSlots = staging_slots<BNMAX>();
+  constexpr int kSlots = staging_slots<BNMAX, LOCALT>();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* staging = reinterpret_cast<float*>(smem + STAGES * kStage);  // [kSlots][bn/4][128][4]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStage + staging_bytes<BNMAX>());
+  uint8_t* tprime = smem + STAGES * kStage;  // [2][BNMAX][128 B] (LOCALT)
+  float* staging = reinterpret_cast<float*>(tprime + tprime_bytes<BNMAX, LOCALT>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(staging) +
+                                               staging_bytes<BNMAX, LOCALT>());
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;  // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;      // [2] accumulator drained
+  uint64_t* tfull = empty + STAGES;  // [2] y accumulator ready
+  uint64_t* tempty = tfull + 2;      // [2] y accumulator drained
   uint64_t* mma_done = tempty + 2;
   uint64_t* stg_bar = mma_done + 1;  // staging area filled
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_bar + 1);
+  uint64_t* t_ready = stg_bar + 1;   // (LOCALT) the piece's T accumulator is complete
+  uint64_t* t_smem = t_ready + 1;    // (LOCALT) T' is in shared memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_smem + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // The schedule is read with run-time indices all through the kernel: keep a
   // copy in shared memory rather than in the (small) constant cache.
@@ -383,8 +429,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
 
-  static_assert((2 * STAGES + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
-  static_assert(smem_bytes_for<BNMAX>() <= 227 * 1024, "shared memory per CTA");
+  static_assert((2 * STAGES + 8) * 8 + 16 <= kBarrierBytes, "barrier area");
+  static_assert(smem_bytes_for<BNMAX, LOCALT>() <= 227 * 1024, "shared memory per CTA");
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -396,6 +442,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     }
     ptx::mbar_init(mma_done, 1);
     ptx::mbar_init(stg_bar, 1);
+    ptx::mbar_init(t_ready, 1);
+    ptx::mbar_init(t_smem, kEpiThreads / 32);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -407,13 +455,40 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_t = tmem + uint32_t(kAcc * BNMAX);  // (LOCALT) T accumulator
+  if (threadIdx.x == 0) ptx::grid_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    // Before the previous launch has finished: L2 prefetch hints for the
+    // weight tiles of this CTA's first K-blocks.
+    int left = kPrefetchKBlocks;
+    for (int sec = 0; sec < 2 && left > 0; ++sec) {
+      const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
+      for (int64_t k = lo; k < hi && left > 0;) {
+        const Seg g = locate(P, sec, k, hi);
+        const Phase& f = P.ph[g.ph];
+        const CUtensorMap* mp = maps.m[f.prob];
+        const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
+        for (int64_t i = 0; i < g.e - g.s && left > 0; ++i, --left) {
+          const int kl = int(piece_kb(g, f.na, i) - g.tstart);
+          if (f.down)
+            ptx::tma_prefetch_l2_2d(&mp[MAP_A], kl * kBK, SWAP ? ta * kBM : tb * f.bn);
+          else if (kl >= f.na)
+            ptx::tma_prefetch_l2_2d(&mp[MAP_W], (kl - f.na) * kBK, SWAP ? ta * kBM : tb * f.bn);
+        }
+        k = g.e;
+      }
+    }
+  }
+  // Everything below may read what the previous launch wrote.
+  ptx::grid_dependency_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       // swap: A = weights (streamed once), B = tokens (reused by every tile);
       // otherwise A = tokens, B = weights, both reused across tiles from L2.
-      const uint64_t polA = P.swap ? ptx::policy_evict_first() : ptx::policy_evict_last();
+      const uint64_t polA = SWAP ? ptx::policy_evict_first() : ptx::policy_evict_last();
       const uint64_t polB = ptx::policy_evict_last();
       uint32_t it = 0;
       for (int sec = 0; sec < 2 && !*abort_flag; ++sec) {
@@ -424,16 +499,18 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
           const Prob& pb = P.pb[f.prob];
           const CUtensorMap* mp = maps.m[f.prob];
           const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
-          const uint32_t bytes = kABytes + uint32_t(f.bn) * kBK * 2;
-          const int64_t n = g.e - g.s;
-          bool t_ready = false;
+          // LOCALT: base K-blocks carry the down slice; then the piece's
+          // adapter K-blocks bring the up-projection's rows (A operand only)
+          const int64_t n = (g.e - g.s) + (LOCALT ? f.nad : 0);
+          bool t_ready_flag = false;
           for (int64_t i = 0; i < n; ++i, ++it) {
-            const int kl = int(piece_kb(g, f.na, i) - g.tstart);
-            const bool adapter = kl < f.na;
-            if (adapter && !t_ready) {
+            const bool local_ad = LOCALT && i >= g.e - g.s;
+            const int kl = local_ad ? 0 : int(piece_kb(g, f.na, i) - g.tstart);
+            const bool adapter = !LOCALT && kl < f.na;
+            if (adapter && !t_ready_flag) {
               // The rows of T this tile reads must be complete before TMA reads them.
               bool ok = true;
-              if (P.swap) {
+              if (SWAP) {
                 for (int j = 0; j < pb.ttiles && ok; ++j)
                   ok = wait_flag(P.tflag + pb.tflag0 + j, kWaitLimitNs);
               } else {
@@ -444,32 +521,41 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                 break;
               }
               fence_proxy_async();
-              t_ready = true;
+              t_ready_flag = true;
             }
             const int s = int(it % STAGES);
             if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitLimitNs)) {
               *abort_flag = 1;
               break;
             }
+            uint8_t* sa = smem + s * kStage;
+            if (local_ad) {
+              const int j = int(i - (g.e - g.s));
+              ptx::mbar_arrive_expect_tx(&full[s], kABytes);
+              ptx::tma_load_2d(sa, &mp[MAP_B], &full[s], j * kBK, ta * kBM, polB);
+              continue;
+            }
             const CUtensorMap *ma, *mb;
             int kc;
             if (f.down) {
-              ma = &mp[P.swap ? MAP_A : MAP_X];
-              mb = &mp[P.swap ? MAP_X : MAP_A];
+              ma = &mp[SWAP ? MAP_A : MAP_X];
+              mb = &mp[SWAP ? MAP_X : MAP_A];
               kc = kl * kBK;
             } else if (!adapter) {
-              ma = &mp[P.swap ? MAP_W : MAP_X];
-              mb = &mp[P.swap ? MAP_X : MAP_W];
+              ma = &mp[SWAP ? MAP_W : MAP_X];
+              mb = &mp[SWAP ? MAP_X : MAP_W];
               kc = (kl - f.na) * kBK;
             } else {
-              ma = &mp[P.swap ? MAP_B : MAP_T];
-              mb = &mp[P.swap ? MAP_T : MAP_B];
+              ma = &mp[SWAP ? MAP_B : MAP_T];
+              mb = &mp[SWAP ? MAP_T : MAP_B];
               kc = kl * kBK;
             }
-            uint8_t* sa = smem + s * kStage;
-            ptx::mbar_arrive_expect_tx(&full[s], bytes);
+            const bool down_slice = LOCALT && pb.r > 0;
+            ptx::mbar_arrive_expect_tx(
+                &full[s], kABytes + uint32_t(f.bn) * kBK * 2 + (down_slice ? kABytes : 0u));
             ptx::tma_load_2d(sa, ma, &full[s], kc, ta * kBM, polA);
             ptx::tma_load_2d(sa + kABytes, mb, &full[s], kc, tb * f.bn, polB);
+            if (down_slice) ptx::tma_load_2d(sa + kABytes + kBSlot, &mp[MAP_A], &full[s], kc, 0, polB);
           }
           k = g.e;
         }
@@ -485,26 +571,29 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      uint32_t it = 0;
+      uint32_t it = 0, tcount = 0;
       int seg = 0;
       for (int sec = 0; sec < 2 && !*abort_flag; ++sec) {
         const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
         for (int64_t k = lo; k < hi && !*abort_flag; ++seg) {
           const Seg g = locate(P, sec, k, hi);
           const Phase& f = P.ph[g.ph];
-          const int acc = seg & 1;
-          if (seg >= 2 && !ptx::mbar_wait(&tempty[acc], ((seg >> 1) - 1) & 1, kWaitLimitNs)) {
+          const Prob& pb = P.pb[f.prob];
+          const int acc = seg % kAcc, use = seg / kAcc;
+          if (seg >= kAcc && !ptx::mbar_wait(&tempty[acc], (use - 1) & 1, kWaitLimitNs)) {
             *abort_flag = 1;
             break;
           }
           ptx::tc_fence_after();
           const uint32_t d = tmem + uint32_t(acc * BNMAX);
           const uint32_t idesc = ptx::idesc_bf16_f32(kBM, f.bn);
-          const int64_t n = g.e - g.s;
-          for (int64_t i = 0; i < n; ++i, ++it) {
+          const bool local_t = LOCALT && pb.r > 0;
+          const int64_t nb = g.e - g.s;
+          bool ok = true;
+          for (int64_t i = 0; i < nb; ++i, ++it) {
             const int s = int(it % STAGES);
             if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, kWaitLimitNs)) {
-              *abort_flag = 1;
+              ok = false;
               break;
             }
             ptx::tc_fence_after();
@@ -514,7 +603,42 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             for (int u = 0; u < kBK / kUmmaK; ++u)
               ptx::umma_f16(d, ptx::sw128_kmajor_desc(sa + u * 32), ptx::sw128_kmajor_desc(sb + u * 32),
                             idesc, (i > 0 || u > 0) ? 1u : 0u);
+            if (local_t) {
+              // this piece's share of T: down slice x tokens, into its own accumulator
+#pragma unroll
+              for (int u = 0; u < kBK / kUmmaK; ++u)
+                ptx::umma_f16(tmem_t, ptx::sw128_kmajor_desc(sb + kBSlot + u * 32),
+                              ptx::sw128_kmajor_desc(sb + u * 32), idesc, (i > 0 || u > 0) ? 1u : 0u);
+            }
             ptx::umma_commit(&empty[s]);
+          }
+          if (ok && local_t) {
+            // T' = bf16(gate * scale * T) comes back through shared memory;
+            // then y += (up-projection rows) . T'^T
+            ptx::umma_commit(t_ready);
+            if (!ptx::mbar_wait(t_smem, tcount & 1, kWaitLimitNs)) ok = false;
+            ++tcount;
+            ptx::tc_fence_after();
+            const uint32_t st = ptx::smem_u32(tprime);
+            for (int j = 0; j < f.nad && ok; ++j, ++it) {
+              const int s = int(it % STAGES);
+              if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              const uint32_t sa = ptx::smem_u32(smem + s * kStage);
+              const uint32_t tb = st + uint32_t(j) * uint32_t(BNMAX) * 128u;
+#pragma unroll
+              for (int u = 0; u < kBK / kUmmaK; ++u)
+                ptx::umma_f16(d, ptx::sw128_kmajor_desc(sa + u * 32), ptx::sw128_kmajor_desc(tb + u * 32),
+                              idesc, 1u);
+              ptx::umma_commit(&empty[s]);
+            }
+          }
+          if (!ok) {
+            *abort_flag = 1;
+            break;
           }
           ptx::umma_commit(&tfull[acc]);
           k = g.e;
@@ -531,6 +655,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     const int row = q * 32 + lane;
     const int et = threadIdx.x - 64;
     uint32_t stg_phase = 0;  // phases of stg_bar used so far
+    uint32_t tcount = 0;     // (swap) T drains so far
     int seg = 0;
     for (int sec = 0; sec < 2; ++sec) {
       const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
@@ -539,17 +664,51 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
         const Phase& f = P.ph[g.ph];
         const Prob& pb = P.pb[f.prob];
         const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
-        const int acc = seg & 1;
+        const int acc = seg % kAcc, use = seg / kAcc;
         const bool whole = g.s == g.tstart && g.e == g.tend;
         const bool finisher = !whole && g.s == g.tstart;
         const int c1 = finisher ? owner_of(P, sec, g.tend - 1) : cta;
-        float pre[kPreMerge ? BNMAX : 1];
         bool fail = false;
+        if (LOCALT && pb.r > 0) {
+          // The piece's T (lane = rank, column = token) becomes T' =
+          // bf16(gate * scale * T) in shared memory, K-major with the 128-byte
+          // swizzle, as the B operand of the up-projection.
+          if (!ptx::mbar_wait(t_ready, tcount & 1, kWaitLimitNs)) fail = true;
+          ++tcount;
+          if (epi_sync_or(fail || *abort_flag)) {
+            *abort_flag = 1;
+            goto done;
+          }
+          ptx::tc_fence_after();
+          if (row < f.nad * kBK) {
+            const uint32_t tq = tmem_t + (uint32_t(q * 32) << 16);
+            uint8_t* tk = tprime + (row >> 6) * (BNMAX * 128);
+            const int jj = row & 63;
+            for (int c0 = 0; c0 < f.bn; c0 += 16) {
+              float v[16];
+              tmem_ld16f(tq + c0, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int m = c0 + j;
+                const float gs = m < P.M ? float(__ldg(pb.gate + m)) * pb.scale : 0.f;
+                const __nv_bfloat16 h = __float2bfloat16_rn(v[j] * gs);
+                *reinterpret_cast<__nv_bfloat16*>(tk + m * 128 + ((((jj >> 3) ^ (m & 7))) << 4) +
+                                                  (jj & 7) * 2) = h;
+              }
+            }
+          }
+          // generic-proxy stores, read next by the tensor cores
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(t_smem);
+        }
+        float pre[kPreMerge ? BNMAX : 1];
         if (finisher) {
           if constexpr (kPreMerge) {
             // While the tensor cores finish this piece, bring the contributors'
-            // partials into shared memory (one bulk copy each, issued as soon as
-            // its flag is up) and sum them in CTA order.
+            // partials into shared memory (one bulk copy each) and sum them in
+            // CTA order.
             const uint32_t bytes = uint32_t(f.bn) * kBM * 4;
             bool any = false;
             int c = cta + 1;
@@ -603,7 +762,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             fail = !wait_ready(P, sec, cta + 1, c1, kWaitLimitNs);
           }
         }
-        if (!ptx::mbar_wait(&tfull[acc], (seg >> 1) & 1, kWaitLimitNs)) fail = true;
+        if (!ptx::mbar_wait(&tfull[acc], use & 1, kWaitLimitNs)) fail = true;
         if (epi_sync_or(fail || *abort_flag)) {
           *abort_flag = 1;
           goto done;
@@ -647,21 +806,21 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
               tmem_ld16f(tq + c0, v);
               for (int cb = cta + 1; cb <= c1; cb += 4) {
                 float4 t[4][4];
-                bool use[4];
+                bool use4[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                   const int c = cb + u;
-                  use[u] = c <= c1 && P.lo[sec][c] < P.lo[sec][c + 1];
+                  use4[u] = c <= c1 && P.lo[sec][c] < P.lo[sec][c + 1];
                   const float4* src = reinterpret_cast<const float4*>(
-                      P.partial + (size_t(use[u] ? c : cta) * 2 + sec) * kSlot);
+                      P.partial + (size_t(use4[u] ? c : cta) * 2 + sec) * kSlot);
 #pragma unroll
                   for (int i = 0; i < 4; ++i)
-                    t[u][i] = use[u] ? __ldcg(src + ((c0 >> 2) + i) * kBM + row)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    t[u][i] = use4[u] ? __ldcg(src + ((c0 >> 2) + i) * kBM + row)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                  if (use[u]) {
+                  if (use4[u]) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                       v[4 * i] += t[u][i].x;
@@ -706,6 +865,14 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Clears the schedule's flags once the previous launch in the stream has
+// finished, letting the projection kernel that follows start right away.
+__global__ void sync_reset_kernel(int* __restrict__ sync, int n) {
+  if (threadIdx.x == 0) ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) sync[i] = 0;
 }
 
 __global__ void cast_f32_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
@@ -765,7 +932,18 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   std::memset(&L, 0, sizeof(L));
   Params& P = L.P;
   P.M = int(M);
+  // Decode-sized M swaps the operands (weights fill the 128-row MMA side).
+  // A short launch (little weight to stream) cannot hide the latency of a
+  // shared T, so each piece then computes its own share of the adapter
+  // (ranks up to 128); a long launch computes T once per T tile.
   P.swap = M <= 256 ? 1 : 0;
+  int64_t wbytes = 0;
+  bool small_rank = true;
+  for (int p = 0; p < n; ++p) {
+    wbytes += 2 * pr[p].d_in * pr[p].d_out;
+    small_rank = small_rank && pr[p].rank <= kMaxLocalRank;
+  }
+  P.localt = (P.swap && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
   P.out_f32 = dtype == UNO_F32;
   const int bn_tok = pick_bn(M);
   int nph = 0, tflags = 0, bnmax = 16, max_down_nkb = 0;
@@ -777,7 +955,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     b.r = int(pr[p].rank);
     b.scale = pr[p].rank > 0 ? pr[p].alpha / float(pr[p].rank) : 0.f;
     b.tflag0 = tflags;
-    if (pr[p].rank == 0) continue;
+    if (pr[p].rank == 0 || P.localt) continue;
     Phase& f = P.ph[nph++];
     f.kb_start = kb;
     f.prob = p;
@@ -803,7 +981,8 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     f.kb_start = kb;
     f.prob = p;
     f.down = 0;
-    f.na = int((pr[p].rank + kBK - 1) / kBK);
+    f.na = P.localt ? 0 : int((pr[p].rank + kBK - 1) / kBK);
+    f.nad = P.localt ? int((pr[p].rank + kBK - 1) / kBK) : 0;
     f.nkb = f.na + int((pr[p].d_in + kBK - 1) / kBK);
     if (P.swap) {
       f.tiles_a = int((pr[p].d_out + kBM - 1) / kBM);
@@ -874,7 +1053,7 @@ cudaError_t cast_to_bf16(const void* in, void* out, int64_t n, cudaStream_t st) 
   return cudaGetLastError();
 }
 
-template <int BNMAX>
+template <int BNMAX, bool SWAP, bool LOCALT>
 cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   static std::once_flag once[64];
   static cudaError_t attr_err[64] = {};
@@ -882,22 +1061,24 @@ cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   cudaGetDevice(&dev);
   dev &= 63;
   std::call_once(once[dev], [&] {
-    attr_err[dev] = cudaFuncSetAttribute(grouped_lora_gemm_kernel<BNMAX>,
+    attr_err[dev] = cudaFuncSetAttribute(grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem_bytes_for<BNMAX>()));
+                                         int(smem_bytes_for<BNMAX, LOCALT>()));
   });
   if (attr_err[dev] != cudaSuccess) return attr_err[dev];
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(P.grid));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes_for<BNMAX>();
+  cfg.dynamicSmemBytes = smem_bytes_for<BNMAX, LOCALT>();
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX>, maps, P);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT>, maps, P);
 }
 
 }  // namespace
@@ -957,15 +1138,38 @@ int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, v
     }
     if (!ok) return UNO_ERR_CUDA;
   }
-  if (cudaMemsetAsync(w + L.off_sync, 0, L.sync_bytes, st) != cudaSuccess) return UNO_ERR_CUDA;
-  cudaError_t e;
-  switch (P.bnmax) {
-    case 16: e = launch_grouped<16>(maps, P, st); break;
-    case 32: e = launch_grouped<32>(maps, P, st); break;
-    case 64: e = launch_grouped<64>(maps, P, st); break;
-    case 128: e = launch_grouped<128>(maps, P, st); break;
-    default: e = launch_grouped<256>(maps, P, st); break;
+  {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sync_reset_kernel, reinterpret_cast<int*>(w + L.off_sync),
+                           int(L.sync_bytes / sizeof(int))) != cudaSuccess)
+      return UNO_ERR_CUDA;
   }
+  cudaError_t e;
+  // one instantiation per (tile width, operand order, adapter mode)
+#define UNO_DISPATCH(SW, LT)                                             \
+  switch (P.bnmax) {                                                     \
+    case 16: e = launch_grouped<16, SW, LT>(maps, P, st); break;         \
+    case 32: e = launch_grouped<32, SW, LT>(maps, P, st); break;         \
+    case 64: e = launch_grouped<64, SW, LT>(maps, P, st); break;         \
+    case 128: e = launch_grouped<128, SW, LT>(maps, P, st); break;       \
+    default: e = launch_grouped<256, SW, LT>(maps, P, st); break;        \
+  }
+  if (P.localt) {
+    UNO_DISPATCH(true, true)
+  } else if (P.swap) {
+    UNO_DISPATCH(true, false)
+  } else {
+    UNO_DISPATCH(false, false)
+  }
+#undef UNO_DISPATCH
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
 
