@@ -66,6 +66,29 @@ def peaks():
         return 6400.0, 1800.0, "fallback"
 
 
+def profiled_traffic(batch, launches):
+    """DRAM bytes per projection launch from the committed ncu summary, or None
+    when there is none for this workload or the kernel sources changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"gemm_traffic_llama3_layer_b{batch}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for name in ("gemm.cu", "ptx.cuh", "uno_internal.h"):
+            with open(os.path.join(ROOT, "lossless_draft_verify_gated_b300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != kv.get("source_sha256_16") or int(kv["launches_per_step"]) != launches:
+            return None
+        return int(kv["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def workload_name(batch):
     return (f"llama3-8b-layer b{batch} k{BLOCK}: 7 gated-LoRA projections M={2 * BLOCK * batch} "
             f"r={RANK} alpha={int(ALPHA)} bf16 + block verifier B={batch} K={BLOCK} V={VOCAB} fp32")
@@ -183,8 +206,9 @@ class Step:
         self.vws = torch.empty(binding.uno_verify_block_workspace(batch, BLOCK, BLOCK, VOCAB),
                                dtype=torch.uint8, device=device)
         self.n_gate1 = int(self.layer[0][1].gate.sum())
-        # kernels of this library per step: one persistent GEMM per group, two for the verifier
-        self.launches_per_step = len(self.groups) + 2
+        # kernels of this library per step: per group a one-CTA flag reset and the
+        # persistent GEMM, then the verifier's two kernels
+        self.launches_per_step = 2 * len(self.groups) + 2
 
     def projections(self):
         from lossless_draft_verify_gated_b300 import binding
@@ -291,7 +315,9 @@ def run_uno(args):
                    "grouping": args.grouping + ": " + " | ".join(",".join(g) for g in GROUPINGS[args.grouping]),
                    "parallelism": f"dp{ws} (independent replicas, no collective)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(args.batch, len(st.groups)),
+                     "algorithmic_bytes_per_launch": by // len(st.groups),
                      "kernel": f"gated-LoRA projections of the layer ({len(st.groups)} persistent grouped GEMM launch(es))",
                      "peak_source": peak_kind, "algorithmic_bytes": by, "algorithmic_flops": fl,
                      "ms": round(ms_proj, 5)},
@@ -385,40 +411,50 @@ class OracleStep:
         self.rows = min(self.M, max(2, self.threads))
         self.seqs = min(batch, max(1, self.threads))
         self.col_frac = 1.0
+        self.repeat = 1  # samples per timed step (a small step is repeated to time it reliably)
 
     def run(self):
         import numpy as np
         import oracle
         M, rows = self.M, self.rows
         r_idx = np.concatenate([np.arange(rows // 2), M - 1 - np.arange(rows - rows // 2)])
-        t0 = time.perf_counter()
-        scale_p = 0.0
-        for _, p in self.layer:
-            d_out = p.W.shape[0]
-            c = max(8, int(round(d_out * self.col_frac / 8)) * 8)
-            c = min(c, d_out)
-            oracle.gated_lora_linear(p.x[r_idx], p.W[:c], p.A, p.B[:c], p.gate[r_idx], p.alpha)
-            scale_p = (M / rows) * (d_out / c)  # equal fractions for every projection
-        t1 = time.perf_counter()
-        s = self.seqs
-        vp = self.vp
-        r = oracle.verify_block(vp.p_logits[:s], vp.q_logits[:s], self.draft[:s], vp.u_accept[:s],
-                                vp.u_resample[:s])
-        t2 = time.perf_counter()
-        t_full = (t1 - t0) * scale_p + (t2 - t1) * (self.batch / s)
+        tp = tv = 0.0
+        for _ in range(self.repeat):
+            t0 = time.perf_counter()
+            scale_p = 0.0
+            for _, p in self.layer:
+                d_out = p.W.shape[0]
+                c = max(8, int(round(d_out * self.col_frac / 8)) * 8)
+                c = min(c, d_out)
+                oracle.gated_lora_linear(p.x[r_idx], p.W[:c], p.A, p.B[:c], p.gate[r_idx], p.alpha)
+                scale_p = (M / rows) * (d_out / c)  # equal fractions for every projection
+            t1 = time.perf_counter()
+            s = self.seqs
+            vp = self.vp
+            r = oracle.verify_block(vp.p_logits[:s], vp.q_logits[:s], self.draft[:s], vp.u_accept[:s],
+                                    vp.u_resample[:s])
+            t2 = time.perf_counter()
+            tp += t1 - t0
+            tv += t2 - t1
+        t_full = (tp * scale_p + tv * (self.batch / s)) / self.repeat
         tokens = float(r.n_emitted.sum()) * (self.batch / s)
-        return t_full, tokens, (t2 - t0)
+        return t_full, tokens, tp + tv
 
     def calibrate(self, target_s):
-        """Pick the column fraction so that one sample takes about target_s."""
-        self.col_frac = 1.0 / 16
+        """Pick the column fraction (and, when the whole step is shorter than
+        target_s, a repeat count) so that one timed sample takes about target_s."""
+        self.col_frac, self.repeat = 1.0 / 16, 1
         _, _, t = self.run()
-        self.col_frac = min(1.0, max(1.0 / 512, self.col_frac * target_s / max(t, 1e-3)))
+        want = self.col_frac * target_s / max(t, 1e-3)
+        self.col_frac = min(1.0, max(1.0 / 512, want))
+        if want > 1.0:  # the whole step is short: time it once and repeat it
+            _, _, t1 = self.run()
+            self.repeat = max(1, min(1000, int(round(target_s / max(t1, 1e-3)))))
 
     def describe(self, steps):
         return (f"{self.rows} of {self.M} rows x {self.col_frac:.4f} of the output columns of each of "
                 f"the 7 projections + the verifier for {self.seqs} of {self.batch} sequences per step, "
-                f"scaled to the full step; {steps} step(s)")
+                f"scaled to the full step, each sample run {self.repeat}x and averaged; {steps} step(s)")
 
 
 def cpu_baseline(st, batch, sigma, budget_s=15.0):
