@@ -71,7 +71,7 @@ constexpr int kUmmaK = 16;  // K of one tcgen05.mma for 16-bit inputs
 constexpr int kThreads = 192;  // warps: 0 TMA, 1 MMA, 2-5 epilogue
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kMaxPhases = 2 * kMaxLoraProblems;
+constexpr int kMaxPhases = 4 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
 constexpr int kPrefetchKBlocks = 24;
 constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;  // weight tiles hinted into L2 before the previous launch ends
@@ -85,7 +85,9 @@ struct Maps {
 
 // A run of equally shaped tiles of one problem inside a section.
 struct Phase {
-  int64_t kb_start;  // first K-block of the phase in its section
+  int64_t kb_start;  // first K-block of the phase in its stream-K section
+  int tile0;         // first tile of the phase in its problem's tile grid
+  int tbase;         // (data-parallel phases) first tile in the combined tile list
   int tiles;
   int tiles_a;       // tiles along the A-operand rows (tile = tb * tiles_a + ta)
   int nkb;           // K-blocks per tile
@@ -110,7 +112,9 @@ struct Prob {
 struct Params {
   Phase ph[kMaxPhases];
   Prob pb[kMaxLoraProblems];
-  int ph0[2], ph1[2];  // section s holds phases [ph0[s], ph1[s])
+  int ph0[2], ph1[2];  // stream-K section s holds phases [ph0[s], ph1[s])
+  int dp0, dp1;        // data-parallel phases [dp0, dp1) (large M)
+  int dp_tiles;        // tiles of the data-parallel waves: tile t goes to CTA t % grid
   int swap;
   int localt;  // swap path with per-piece adapter
   int M;
@@ -186,8 +190,10 @@ __host__ __device__ constexpr uint32_t smem_bytes_for() {
          1024;
 }
 
+// A piece: K-blocks [s, e) of tile `tile` (whose K-blocks are [tstart, tend)),
+// in stream-K section `sec`, or a whole data-parallel tile (sec = -1).
 struct Seg {
-  int ph, tile;
+  int ph, tile, sec;
   int64_t tstart, tend, s, e;
 };
 
@@ -196,14 +202,51 @@ __device__ __forceinline__ Seg locate(const Params& P, int sec, int64_t k, int64
   int p = P.ph0[sec];
   while (p + 1 < P.ph1[sec] && P.ph[p + 1].kb_start <= k) ++p;
   const Phase& f = P.ph[p];
+  const int local = int((k - f.kb_start) / f.nkb);
   g.ph = p;
-  g.tile = int((k - f.kb_start) / f.nkb);
-  g.tstart = f.kb_start + int64_t(g.tile) * f.nkb;
+  g.sec = sec;
+  g.tile = f.tile0 + local;
+  g.tstart = f.kb_start + int64_t(local) * f.nkb;
   g.tend = g.tstart + f.nkb;
   g.s = k;
   g.e = hi < g.tend ? hi : g.tend;
   return g;
 }
+
+// The pieces of one CTA, in order: its data-parallel tiles (t = cta, cta +
+// grid, ...), then its ranges of the two stream-K sections.
+struct PieceIter {
+  int t, sec;
+  int64_t k, hi;
+  __device__ __forceinline__ PieceIter(const Params& P, int cta)
+      : t(cta), sec(0), k(P.lo[0][cta]), hi(P.lo[0][cta + 1]) {}
+  __device__ __forceinline__ bool next(const Params& P, int cta, Seg& g) {
+    if (t < P.dp_tiles) {
+      int p = P.dp0;
+      while (p + 1 < P.dp1 && P.ph[p + 1].tbase <= t) ++p;
+      const Phase& f = P.ph[p];
+      g.ph = p;
+      g.sec = -1;
+      g.tile = f.tile0 + (t - f.tbase);
+      g.tstart = g.s = 0;
+      g.tend = g.e = f.nkb;
+      t += P.grid;
+      return true;
+    }
+    while (sec < 2) {
+      if (k < hi) {
+        g = locate(P, sec, k, hi);
+        k = g.e;
+        return true;
+      }
+      if (++sec < 2) {
+        k = P.lo[sec][cta];
+        hi = P.lo[sec][cta + 1];
+      }
+    }
+    return false;
+  }
+};
 
 // Flat position of the i-th K-block a CTA runs in piece g: base K-blocks
 // first, then the adapter K-blocks (flat positions [tstart, tstart + na)).
@@ -462,10 +505,10 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     // Before the previous launch has finished: L2 prefetch hints for the
     // weight tiles of this CTA's first K-blocks.
     int left = kPrefetchKBlocks;
-    for (int sec = 0; sec < 2 && left > 0; ++sec) {
-      const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
-      for (int64_t k = lo; k < hi && left > 0;) {
-        const Seg g = locate(P, sec, k, hi);
+    PieceIter pit(P, cta);
+    Seg g;
+    while (left > 0 && pit.next(P, cta, g)) {
+      {
         const Phase& f = P.ph[g.ph];
         const CUtensorMap* mp = maps.m[f.prob];
         const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
@@ -476,7 +519,6 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
           else if (kl >= f.na)
             ptx::tma_prefetch_l2_2d(&mp[MAP_W], (kl - f.na) * kBK, SWAP ? ta * kBM : tb * f.bn);
         }
-        k = g.e;
       }
     }
   }
@@ -491,10 +533,10 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
       const uint64_t polA = SWAP ? ptx::policy_evict_first() : ptx::policy_evict_last();
       const uint64_t polB = ptx::policy_evict_last();
       uint32_t it = 0;
-      for (int sec = 0; sec < 2 && !*abort_flag; ++sec) {
-        const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
-        for (int64_t k = lo; k < hi && !*abort_flag;) {
-          const Seg g = locate(P, sec, k, hi);
+      PieceIter pit(P, cta);
+      Seg g;
+      while (!*abort_flag && pit.next(P, cta, g)) {
+        {
           const Phase& f = P.ph[g.ph];
           const Prob& pb = P.pb[f.prob];
           const CUtensorMap* mp = maps.m[f.prob];
@@ -557,7 +599,6 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             ptx::tma_load_2d(sa + kABytes, mb, &full[s], kc, tb * f.bn, polB);
             if (down_slice) ptx::tma_load_2d(sa + kABytes + kBSlot, &mp[MAP_A], &full[s], kc, 0, polB);
           }
-          k = g.e;
         }
       }
       if (*abort_flag) {
@@ -573,10 +614,10 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
       // ------------------------------------------------------------ MMA issuer
       uint32_t it = 0, tcount = 0;
       int seg = 0;
-      for (int sec = 0; sec < 2 && !*abort_flag; ++sec) {
-        const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
-        for (int64_t k = lo; k < hi && !*abort_flag; ++seg) {
-          const Seg g = locate(P, sec, k, hi);
+      PieceIter pit(P, cta);
+      Seg g;
+      for (; !*abort_flag && pit.next(P, cta, g); ++seg) {
+        {
           const Phase& f = P.ph[g.ph];
           const Prob& pb = P.pb[f.prob];
           const int acc = seg % kAcc, use = seg / kAcc;
@@ -641,7 +682,6 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             break;
           }
           ptx::umma_commit(&tfull[acc]);
-          k = g.e;
         }
       }
       // once this arrives, every MMA issued by this thread has completed
@@ -657,10 +697,11 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     uint32_t stg_phase = 0;  // phases of stg_bar used so far
     uint32_t tcount = 0;     // (swap) T drains so far
     int seg = 0;
-    for (int sec = 0; sec < 2; ++sec) {
-      const int64_t lo = P.lo[sec][cta], hi = P.lo[sec][cta + 1];
-      for (int64_t k = lo; k < hi; ++seg) {
-        const Seg g = locate(P, sec, k, hi);
+    PieceIter pit(P, cta);
+    Seg g;
+    for (; pit.next(P, cta, g); ++seg) {
+      const int sec = g.sec;
+      {
         const Phase& f = P.ph[g.ph];
         const Prob& pb = P.pb[f.prob];
         const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
@@ -852,7 +893,6 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             }
           }
         }
-        k = g.e;
       }
     }
   done:;
@@ -946,21 +986,22 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   P.localt = (P.swap && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
   P.out_f32 = dtype == UNO_F32;
   const int bn_tok = pick_bn(M);
-  int nph = 0, tflags = 0, bnmax = 16, max_down_nkb = 0;
-  int64_t kb = 0;
-  P.ph0[kDown] = 0;
-  for (int p = 0; p < n; ++p) {  // down section: T tiles of every adapted problem
+
+  // Tile list: the T tiles of every adapted problem (unless each piece makes
+  // its own), then the y tiles of every problem.
+  Phase tl[2 * kMaxLoraProblems];
+  int nt = 0, tflags = 0, bnmax = 16, max_down_nkb = 0;
+  int64_t total_kb = 0, tiles_total = 0;
+  for (int p = 0; p < n; ++p) {
     Prob& b = P.pb[p];
     b.d_out = int(pr[p].d_out);
     b.r = int(pr[p].rank);
     b.scale = pr[p].rank > 0 ? pr[p].alpha / float(pr[p].rank) : 0.f;
     b.tflag0 = tflags;
     if (pr[p].rank == 0 || P.localt) continue;
-    Phase& f = P.ph[nph++];
-    f.kb_start = kb;
+    Phase f{};
     f.prob = p;
     f.down = 1;
-    f.na = 0;
     f.nkb = int((pr[p].d_in + kBK - 1) / kBK);
     // one tile along N: bn covers every token (swap) or the whole rank
     f.tiles_a = int(((P.swap ? pr[p].rank : M) + kBM - 1) / kBM);
@@ -968,19 +1009,13 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     f.tiles = f.tiles_a;
     b.ttiles = f.tiles;
     tflags += f.tiles;
-    kb += int64_t(f.tiles) * f.nkb;
-    bnmax = std::max(bnmax, f.bn);
     max_down_nkb = std::max(max_down_nkb, f.nkb);
+    tl[nt++] = f;
   }
-  P.ph1[kDown] = nph;
-  const int64_t D = kb;
-  P.ph0[kMain] = nph;
-  kb = 0;
-  for (int p = 0; p < n; ++p) {  // main section: y tiles
-    Phase& f = P.ph[nph++];
-    f.kb_start = kb;
+  const int n_down = nt;
+  for (int p = 0; p < n; ++p) {
+    Phase f{};
     f.prob = p;
-    f.down = 0;
     f.na = P.localt ? 0 : int((pr[p].rank + kBK - 1) / kBK);
     f.nad = P.localt ? int((pr[p].rank + kBK - 1) / kBK) : 0;
     f.nkb = f.na + int((pr[p].d_in + kBK - 1) / kBK);
@@ -993,16 +1028,51 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
       f.bn = pick_bn(pr[p].d_out);
       f.tiles = f.tiles_a * int((pr[p].d_out + f.bn - 1) / f.bn);
     }
-    kb += int64_t(f.tiles) * f.nkb;
-    bnmax = std::max(bnmax, f.bn);
+    tl[nt++] = f;
   }
-  P.ph1[kMain] = nph;
-  const int64_t Mn = kb, Wt = D + Mn;
+  for (int i = 0; i < nt; ++i) {
+    tl[i].tbase = int(tiles_total);
+    tiles_total += tl[i].tiles;
+    total_kb += int64_t(tl[i].tiles) * tl[i].nkb;
+    bnmax = std::max(bnmax, tl[i].bn);
+  }
   P.bnmax = bnmax;
   L.tflags = tflags;
   // One CTA per SM, at least 4 K-blocks each.
-  const int G = int(std::max<int64_t>(1, std::min<int64_t>(std::min(sms, kMaxGrid), Wt / 4)));
+  const int G = int(std::max<int64_t>(1, std::min<int64_t>(std::min(sms, kMaxGrid), total_kb / 4)));
   P.grid = G;
+
+  // Large M: whole tiles in data-parallel waves (tile t to CTA t % G, so the
+  // tiles in flight at once share their operands in L2) except for a last
+  // half to one and a half waves' worth of tiles, which stream-K balances.
+  // Decode M: everything is stream-K (there are fewer tiles than CTAs).
+  int nph = 0;
+  int64_t dp_tiles = 0;
+  if (!P.swap) {
+    dp_tiles = std::max<int64_t>(0, (tiles_total - G / 2) / G) * G;
+    P.dp0 = nph;
+    for (int i = 0; i < nt; ++i) P.ph[nph++] = tl[i];
+    P.dp1 = nph;
+  }
+  P.dp_tiles = int(dp_tiles);
+  // Stream-K sections over the remaining tiles: 0 = T tiles, 1 = y tiles.
+  int64_t sec_kb[2] = {0, 0};
+  for (int sec = 0; sec < 2; ++sec) {
+    P.ph0[sec] = nph;
+    for (int i = sec ? n_down : 0; i < (sec ? nt : n_down); ++i) {
+      const int64_t first = std::max<int64_t>(tl[i].tbase, dp_tiles);
+      const int64_t last = int64_t(tl[i].tbase) + tl[i].tiles;
+      if (first >= last) continue;
+      Phase f = tl[i];
+      f.tile0 = int(first - tl[i].tbase);
+      f.tiles = int(last - first);
+      f.kb_start = sec_kb[sec];
+      sec_kb[sec] += int64_t(f.tiles) * f.nkb;
+      P.ph[nph++] = f;
+    }
+    P.ph1[sec] = nph;
+  }
+  const int64_t D = sec_kb[kDown], Mn = sec_kb[kMain], Wt = D + Mn;
   // Down section: a few K-blocks per CTA so that T is complete early, but a
   // T tile in at most 16 pieces (a long d_in takes longer pieces); at large
   // M, where T tiles are many and cheap, whole tiles up to half a CTA's share.
@@ -1014,7 +1084,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   }
   for (int c = 0; c <= G; ++c) P.lo[kDown][c] = c <= Gd && Gd > 0 ? int64_t(c) * D / Gd : D;
   // Main section: CTA c's range ends where the first c+1 CTAs have streamed
-  // (c+1)/G of all K-blocks, down ones included.
+  // (c+1)/G of the section's K-blocks, down ones included.
   P.lo[kMain][0] = 0;
   for (int c = 1; c < G; ++c) {
     const int64_t v = int64_t(c) * Wt / G - P.lo[kDown][c];
