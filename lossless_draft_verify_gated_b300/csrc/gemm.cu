@@ -33,12 +33,13 @@
 // resident.  A main tile's adapter K-blocks wait for the flags of the T
 // tiles they read.
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA (cp.async.bulk.tensor,
-// 128-byte swizzle) into a STAGES-deep shared-memory ring; warp 1 owns TMEM
-// and its lane 0 issues tcgen05.mma (M=128, N=bn, K=16, bf16 -> fp32) into
-// one of two TMEM accumulators; warps 2-5 drain the other accumulator
-// (tcgen05.ld) and store y, T or partials, overlapping the next piece's MMAs.
-// Decode-sized M (<= 256 token rows) swaps the operands so that the weights
+// Roles (224 threads): lane 0 of warps 0 and 6 issue TMA (cp.async.bulk.tensor,
+// 128-byte swizzle) into the even and odd stages of a shared-memory ring;
+// warp 1 owns TMEM and its lane 0 issues tcgen05.mma (M=128, N=bn, K=16,
+// bf16 -> fp32) into one of two TMEM accumulators; warps 2-5 drain the other
+// accumulator (tcgen05.ld) and store y, T or partials, overlapping the next
+// piece's MMAs.
+// Decode-sized M (<= 128 token rows) swaps the operands so that the weights
 // fill the 128-row MMA side and the tokens are N.
 // Launches are chained with programmatic dependent launch: each CTA lets the
 // next launch in the stream start at once, and waits (griddepcontrol.wait)
@@ -68,13 +69,14 @@ namespace {
 constexpr int kBM = 128;    // MMA M: A-operand rows per tile (= TMEM lanes)
 constexpr int kBK = 64;     // K elements per K-block (one 128-byte swizzle row of bf16)
 constexpr int kUmmaK = 16;  // K of one tcgen05.mma for 16-bit inputs
-constexpr int kThreads = 192;  // warps: 0 TMA, 1 MMA, 2-5 epilogue
+constexpr int kThreads = 224;  // warps: 0 and 6 TMA, 1 MMA, 2-5 epilogue
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 4 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
 constexpr int kPrefetchKBlocks = 24;
-constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;  // weight tiles hinted into L2 before the previous launch ends
+constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;
+constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand  // weight tiles hinted into L2 before the previous launch ends
 constexpr int kDown = 0, kMain = 1;
 
 enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, kMapsPerProblem = 5 };
@@ -89,7 +91,8 @@ struct Phase {
   int tile0;         // first tile of the phase in its problem's tile grid
   int tbase;         // (data-parallel phases) first tile in the combined tile list
   int tiles;
-  int tiles_a;       // tiles along the A-operand rows (tile = tb * tiles_a + ta)
+  int tiles_a;       // tiles along the A-operand rows
+  int tiles_all;     // tiles of the problem's whole grid (tiles_a x tiles along B)
   int nkb;           // K-blocks per tile
   int na;            // of which adapter K-blocks, first in the flat order (large-M path)
   int nad;           // adapter K-blocks appended to every piece (swap path)
@@ -211,6 +214,20 @@ __device__ __forceinline__ Seg locate(const Params& P, int sec, int64_t k, int64
   g.s = k;
   g.e = hi < g.tend ? hi : g.tend;
   return g;
+}
+
+// Tile coordinates (A-operand rows ta, B-operand rows tb) of tile `tile` of a
+// phase.  Tiles run through bands of up to 16 A-row tiles, all B-row tiles
+// of a band before the next band, so that the tiles of a wave in flight
+// share a compact set of operand tiles in L2.
+__device__ __forceinline__ void tile_coords(const Phase& f, int tile, int& ta, int& tb) {
+  const int tiles_b = f.tiles_all / f.tiles_a;
+  const int S = f.tiles_a < 16 ? f.tiles_a : 16;
+  const int band = tile / (S * tiles_b);
+  const int r = tile - band * S * tiles_b;
+  const int rows = f.tiles_a - band * S < S ? f.tiles_a - band * S : S;
+  ta = band * S + r % rows;
+  tb = r / rows;
 }
 
 // The pieces of one CTA, in order: its data-parallel tiles (t = cta, cta +
@@ -511,7 +528,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
       {
         const Phase& f = P.ph[g.ph];
         const CUtensorMap* mp = maps.m[f.prob];
-        const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
+        int ta, tb;
+        tile_coords(f, g.tile, ta, tb);
         for (int64_t i = 0; i < g.e - g.s && left > 0; ++i, --left) {
           const int kl = int(piece_kb(g, f.na, i) - g.tstart);
           if (f.down)
@@ -525,9 +543,13 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
   // Everything below may read what the previous launch wrote.
   ptx::grid_dependency_wait();
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------------------------ producers
+      // Two threads in two warps share the ring: warp 0 fills the even
+      // stages, warp 6 the odd ones (one issuing thread sustains only so
+      // many copies in flight).
+      const uint32_t mine = warp == 0 ? 0u : 1u;
       // swap: A = weights (streamed once), B = tokens (reused by every tile);
       // otherwise A = tokens, B = weights, both reused across tiles from L2.
       const uint64_t polA = SWAP ? ptx::policy_evict_first() : ptx::policy_evict_last();
@@ -540,7 +562,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
           const Phase& f = P.ph[g.ph];
           const Prob& pb = P.pb[f.prob];
           const CUtensorMap* mp = maps.m[f.prob];
-          const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
+          int ta, tb;
+        tile_coords(f, g.tile, ta, tb);
           // LOCALT: base K-blocks carry the down slice; then the piece's
           // adapter K-blocks bring the up-projection's rows (A operand only)
           const int64_t n = (g.e - g.s) + (LOCALT ? f.nad : 0);
@@ -549,6 +572,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             const bool local_ad = LOCALT && i >= g.e - g.s;
             const int kl = local_ad ? 0 : int(piece_kb(g, f.na, i) - g.tstart);
             const bool adapter = !LOCALT && kl < f.na;
+            if ((it & 1u) != mine) continue;  // the other producer's stage
             if (adapter && !t_ready_flag) {
               // The rows of T this tile reads must be complete before TMA reads them.
               bool ok = true;
@@ -605,7 +629,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
         // let copies already in flight land before the CTA can exit
         const uint32_t first = it > uint32_t(STAGES) ? it - STAGES : 0;
         for (uint32_t i = first; i < it; ++i)
-          ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kWaitLimitNs);
+          if ((i & 1u) == mine) ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kWaitLimitNs);
       }
     }
     __syncwarp();
@@ -704,7 +728,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
       {
         const Phase& f = P.ph[g.ph];
         const Prob& pb = P.pb[f.prob];
-        const int ta = g.tile % f.tiles_a, tb = g.tile / f.tiles_a;
+        int ta, tb;
+        tile_coords(f, g.tile, ta, tb);
         const int acc = seg % kAcc, use = seg / kAcc;
         const bool whole = g.s == g.tstart && g.e == g.tend;
         const bool finisher = !whole && g.s == g.tstart;
@@ -976,7 +1001,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   // A short launch (little weight to stream) cannot hide the latency of a
   // shared T, so each piece then computes its own share of the adapter
   // (ranks up to 128); a long launch computes T once per T tile.
-  P.swap = M <= 256 ? 1 : 0;
+  P.swap = M <= kSwapMaxRows ? 1 : 0;
   int64_t wbytes = 0;
   bool small_rank = true;
   for (int p = 0; p < n; ++p) {
@@ -1006,7 +1031,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     // one tile along N: bn covers every token (swap) or the whole rank
     f.tiles_a = int(((P.swap ? pr[p].rank : M) + kBM - 1) / kBM);
     f.bn = P.swap ? bn_tok : pick_bn(pr[p].rank);
-    f.tiles = f.tiles_a;
+    f.tiles = f.tiles_all = f.tiles_a;
     b.ttiles = f.tiles;
     tflags += f.tiles;
     max_down_nkb = std::max(max_down_nkb, f.nkb);
@@ -1028,6 +1053,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
       f.bn = pick_bn(pr[p].d_out);
       f.tiles = f.tiles_a * int((pr[p].d_out + f.bn - 1) / f.bn);
     }
+    f.tiles_all = f.tiles;
     tl[nt++] = f;
   }
   for (int i = 0; i < nt; ++i) {
@@ -1043,13 +1069,14 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   P.grid = G;
 
   // Large M: whole tiles in data-parallel waves (tile t to CTA t % G, so the
-  // tiles in flight at once share their operands in L2) except for a last
-  // half to one and a half waves' worth of tiles, which stream-K balances.
-  // Decode M: everything is stream-K (there are fewer tiles than CTAs).
+  // tiles in flight at once share their operands in L2).  Merging a split
+  // 128 x 256 tile costs more than the idle part of a last wave, so a launch
+  // with at least a wave of tiles splits none; fewer tiles than CTAs, and
+  // every decode launch, use stream-K.
   int nph = 0;
   int64_t dp_tiles = 0;
   if (!P.swap) {
-    dp_tiles = std::max<int64_t>(0, (tiles_total - G / 2) / G) * G;
+    dp_tiles = tiles_total >= G ? tiles_total : 0;
     P.dp0 = nph;
     for (int i = 0; i < nt; ++i) P.ph[nph++] = tl[i];
     P.dp1 = nph;
