@@ -29,9 +29,9 @@
 // they leave it as an fp32 partial and raise a flag.  The finisher adds the
 // partials in CTA order to its own accumulator (deterministic).  Every wait
 // points at a CTA with a higher index or at a flag raised before any wait of
-// its raiser, so waits always end; the launch is cooperative so all CTAs are
-// resident.  A main tile's adapter K-blocks wait for the flags of the T
-// tiles they read.
+// its raiser, so waits always end once all CTAs are resident (see
+// launch_grouped).  A main tile's adapter K-blocks wait for the flags of the
+// T tiles they read.
 //
 // Roles (224 threads): lane 0 of warps 0 and 6 issue TMA (cp.async.bulk.tensor,
 // 128-byte swizzle) into the even and odd stages of a shared-memory ring;
@@ -491,6 +491,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
 
   static_assert((2 * STAGES + 8) * 8 + 16 <= kBarrierBytes, "barrier area");
   static_assert(smem_bytes_for<BNMAX, LOCALT>() <= 227 * 1024, "shared memory per CTA");
+  // one CTA per SM: the schedule's waits rely on it (see launch_grouped)
+  static_assert(smem_bytes_for<BNMAX, LOCALT>() > 114 * 1024, "more than half an SM's shared memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -1168,13 +1170,17 @@ cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem_bytes_for<BNMAX, LOCALT>();
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  // Not a cooperative launch: the grid is at most one CTA per SM (each CTA
+  // takes more than half of an SM's shared memory), every wait points at a
+  // higher CTA of this grid or at a flag raised without waiting, and a launch
+  // chained after this one starts only once all of this grid's CTAs have
+  // started (they trigger at entry), so all CTAs become resident without the
+  // guarantee -- and the next launch can take each SM as soon as it is freed.
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT>, maps, P);
 }
 

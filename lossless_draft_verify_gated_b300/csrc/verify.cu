@@ -31,9 +31,16 @@
 namespace uno {
 namespace {
 
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 4;  // float4 loads in flight per thread in the statistics pass
 
 struct MS {
   float m, s;  // running max and sum of exp(x - m)
@@ -90,6 +97,10 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const int64_t per_seq = Kp + K;
   const int64_t b = row / per_seq;
   const int64_t j = row - b * per_seq;
+  // The finish kernel may start once every earlier launch has finished; it
+  // waits for this one before it reads what this one writes.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   if (j == 0 && split == 0 && threadIdx.x == 0) counter[b] = 0;  // finish kernel's arrival count
   // The drafted token of this row's position (AR row j or draft row j - Kp);
   // the thread that streams its logit keeps it for the acceptance test.
@@ -197,11 +208,28 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   __shared__ int s_last;
   __shared__ Cand s_cr[kWarps], s_cp[kWarps];
 
+  constexpr int kRaceUnroll = 4;
   const int tid = threadIdx.x;
   const int64_t b = blockIdx.x / race_splits;
   const int split = int(blockIdx.x - b * race_splits);
   const int64_t per_seq = Kp + K;
+  // Inputs the statistics pass does not write, read before waiting for it:
+  // this thread's drafted token and accept uniform (K <= kThreads) and its
+  // first batch of race uniforms.
+  const bool has_i = tid < K;
+  const int32_t x_t = has_i ? draft[b * K + tid] : 0;
+  const float ua_t = has_i ? u_acc[b * K + tid] : 0.f;
+  const float* ub = u_res + b * V;
+  const int64_t v0 = int64_t(split) * race_chunk;
+  const int64_t v1 = min(V, v0 + race_chunk);
+  float u_pre[kRaceUnroll];
+#pragma unroll
+  for (int i = 0; i < kRaceUnroll; ++i) {
+    const int64_t vi = v0 + tid + int64_t(i) * kThreads;
+    u_pre[i] = vi < v1 ? ub[vi] : 0.5f;
+  }
   if (tid == 0) s_bad = 0;
+  grid_dependency_wait();  // the statistics pass's partials, gathered logits and counters
   __syncthreads();
 
   // 1. Row normalisers of this sequence from the statistics partials: one
@@ -244,10 +272,7 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
     }
   }
   // 2. Draft ids and acceptance flags.
-  for (int64_t i = tid; i < K; i += kThreads) {
-    const int32_t x = draft[b * K + i];
-    if (x < 0 || x >= V) atomicOr(&s_bad, 1);
-  }
+  if (has_i && (x_t < 0 || x_t >= V)) atomicOr(&s_bad, 1);
   __syncthreads();
   const int bad = s_bad;
   int32_t* out = out_tokens + b * (K + 1);
@@ -266,7 +291,8 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   // log domain so that neither probability underflows.
   if (tid == 0) s_n = int(K);
   __syncthreads();
-  for (int64_t i = tid; i < K; i += kThreads) {
+  if (has_i) {
+    const int i = tid;
     // logits of the drafted token, gathered by the statistics pass
     const float lq = gathered[b * per_seq + Kp + i];
     bool accept;
@@ -276,9 +302,9 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       const float lp = gathered[b * per_seq + i];
       const float lr = (lp - s_lz[i]) - (lq - s_lz[Kp + i]);
       const float thr = fminf(1.0f, expf(lr));
-      accept = u_acc[b * K + i] < thr;
+      accept = ua_t < thr;
     }
-    if (!accept) atomicMin(&s_n, int(i));
+    if (!accept) atomicMin(&s_n, i);
   }
   __syncthreads();
   const int n = s_n;
@@ -287,7 +313,7 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const bool bonus = !residual && Kp == K + 1;
   if (!residual && !bonus) {
     if (split == 0) {
-      for (int64_t i = tid; i <= K; i += kThreads) out[i] = i < K ? draft[b * K + i] : -1;
+      for (int64_t i = tid; i <= K; i += kThreads) out[i] = i < K ? x_t : -1;
       if (tid == 0) {
         n_acc[b] = n;
         n_emit[b] = n;
@@ -305,23 +331,20 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const float* qr = q + (b * K + n) * V;  // only read when residual
   const float mp = s_m[prow], izp = s_iz[prow];
   const float mq = residual ? s_m[Kp + n] : 0.f, izq = residual ? s_iz[Kp + n] : 0.f;
-  const float* ub = u_res + b * V;
-  const int64_t v0 = int64_t(split) * race_chunk;
-  const int64_t v1 = min(V, v0 + race_chunk);
   // Each thread keeps its best score as a fraction num/den and compares by
   // cross-multiplication (den = -ln u > 0), dividing once at the end;
   // probabilities come from exp2 of the scaled, max-shifted logit.
   constexpr float kLog2e = 1.4426950408889634f;
   float pn = -1.f, pd = 1.f, rn = 0.f, rd = 1.f;
   int pvid = -1, rvid = -1;
-  constexpr int kRaceUnroll = 4;
   for (int64_t v = v0 + tid; v < v1; v += int64_t(kThreads) * kRaceUnroll) {
     float uu[kRaceUnroll], lp[kRaceUnroll], lq[kRaceUnroll];
+    const bool first = v == v0 + tid;
 #pragma unroll
     for (int i = 0; i < kRaceUnroll; ++i) {
       const int64_t vi = v + int64_t(i) * kThreads;
       const bool in = vi < v1;
-      uu[i] = in ? ub[vi] : 0.5f;
+      uu[i] = first ? u_pre[i] : (in ? ub[vi] : 0.5f);
       lp[i] = in ? pr[vi] : -INFINITY;
       lq[i] = (in && residual) ? qr[vi] : -INFINITY;
     }
@@ -409,7 +432,7 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   __syncthreads();
   const int tok = s_n;
   for (int64_t i = tid; i <= K; i += kThreads)
-    out[i] = i < n ? draft[b * K + i] : (i == n ? tok : -1);
+    out[i] = i < n ? x_t : (i == n ? tok : -1);
 }
 
 // One CTA per row: Gumbel-max form of the race, argmax_v l_v - ln(-ln u_v),
@@ -453,19 +476,20 @@ draft_sample_kernel(const float* __restrict__ logits, const float* __restrict__ 
 VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   VerifyPlan pl{};
   pl.rows = Bn * (Kp + K);
-  // Statistics pass: about 4 CTAs of 256 threads per SM; split rows only
-  // while each chunk keeps at least 4096 logits.
-  const int64_t target = int64_t(sms) * 4;
+  // Statistics pass: about 8 CTAs of 256 threads per SM; split rows only
+  // while each chunk keeps at least 2048 logits.
+  const int64_t target = int64_t(sms) * 8;
   int64_t s = pl.rows > 0 ? (target + pl.rows - 1) / pl.rows : 1;
-  s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 4095) / 4096));
+  s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 2047) / 2048));
   int64_t chunk = (V + s - 1) / s;
   chunk = (chunk + 3) & ~int64_t(3);
   pl.chunk = chunk;
   pl.splits = int((V + chunk - 1) / chunk);
-  // Race pass: about 4 CTAs per SM, chunks of at least 4096 entries.
+  // Race pass: about 4 CTAs per SM, chunks of at least 1024 entries (one
+  // batch of loads per thread at small batch).
   const int64_t rt = int64_t(sms) * 4;
   int64_t s2 = Bn > 0 ? (rt + Bn - 1) / Bn : 1;
-  s2 = std::max<int64_t>(1, std::min<int64_t>(s2, (V + 4095) / 4096));
+  s2 = std::max<int64_t>(1, std::min<int64_t>(s2, (V + 1023) / 1024));
   pl.race_chunk = (V + s2 - 1) / s2;
   pl.race_splits = int((V + pl.race_chunk - 1) / pl.race_chunk);
   pl.off_stats = 0;
