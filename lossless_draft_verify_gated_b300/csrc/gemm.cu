@@ -74,7 +74,7 @@ constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 4 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
-constexpr int kPrefetchKBlocks = 24;
+constexpr int kPrefetchKBlocks = 8;
 constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;
 constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand  // weight tiles hinted into L2 before the previous launch ends
 constexpr int kDown = 0, kMain = 1;
@@ -140,6 +140,7 @@ struct Params {
 constexpr int kMaxStages = 10;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // one 128 x 64 bf16 sub-tile
 constexpr int kMaxLocalRank = 128;           // LOCALT keeps T' for ranks <= 128
+constexpr int64_t kSharedTStaging = 96 * 1024;  // staging of decode tiles with a shared T
 
 template <int BNMAX>
 __host__ __device__ constexpr bool pre_merge() {
@@ -147,7 +148,7 @@ __host__ __device__ constexpr bool pre_merge() {
 }
 template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t staging_bytes() {
-  return pre_merge<BNMAX>() ? (LOCALT ? 32u : 96u) * 1024 : 0u;
+  return pre_merge<BNMAX>() ? (LOCALT ? 32u * 1024 : uint32_t(kSharedTStaging)) : 0u;
 }
 template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr int staging_slots() {  // partials the staging area holds at once
@@ -1103,11 +1104,14 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   }
   const int64_t D = sec_kb[kDown], Mn = sec_kb[kMain], Wt = D + Mn;
   // Down section: a few K-blocks per CTA so that T is complete early, but a
-  // T tile in at most 16 pieces (a long d_in takes longer pieces); at large
-  // M, where T tiles are many and cheap, whole tiles up to half a CTA's share.
+  // T tile in no more pieces than its finisher's staging area holds at once
+  // (one round of bulk copies); at large M, where T tiles are many and cheap,
+  // whole tiles up to half a CTA's share.
   int Gd = 0;
   if (D > 0) {
-    int64_t kd = std::max<int64_t>(4, (max_down_nkb + 15) / 16);
+    const int64_t slots =
+        bnmax <= 64 ? std::max<int64_t>(1, kSharedTStaging / (int64_t(bnmax) * kBM * 4)) : 16;
+    int64_t kd = std::max<int64_t>(4, (max_down_nkb + slots - 1) / slots);
     if (!P.swap) kd = std::max<int64_t>(kd, std::min<int64_t>(max_down_nkb, Wt / G / 2));
     Gd = int(std::max<int64_t>(1, std::min<int64_t>(G, (D + kd - 1) / kd)));
   }
