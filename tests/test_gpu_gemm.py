@@ -39,7 +39,7 @@ def _ref(pr, rows=None):
     (13, 200, 136, 24, 48.0, torch.bfloat16, 4),    # ragged M, K tail, N tail, rank not /64
     (32, 4096, 1024, 128, 256.0, torch.bfloat16, 16),  # k/v projection shape at decode M
     (100, 512, 384, 128, 256.0, torch.bfloat16, 16),   # swap path, 128-wide token tile
-    (256, 1024, 520, 64, 128.0, torch.bfloat16, 16),   # largest swap tile
+    (256, 1024, 520, 64, 128.0, torch.bfloat16, 16),   # large-M order, fewer tiles than CTAs
     (300, 512, 1000, 128, 256.0, torch.bfloat16, 16),  # non-swap path, ragged M and N
     (40, 64, 64, 8, 16.0, torch.bfloat16, 16),         # single K-block
 ])
@@ -80,6 +80,32 @@ def test_llama3_layer_large_m_sampled(M, name, d_in, d_out):
     ref = _ref(pr, rows)
     assert gemm_err(y[rows.cuda()], ref) <= GEMM_TOL
     assert pr.gate[rows].sum() > 0 and (pr.gate[rows] == 0).sum() > 0
+
+
+@pytest.mark.parametrize("M", [64, 128, 129, 255])
+def test_operand_order_boundaries(M):
+    """Both sides of the decode/large-M switch (tokens as the MMA N side up to
+    128 rows, as its M side above) and the per-piece adapter at N = 64 and
+    N = 128: a q-shaped projection alone (per-piece T) and the gate/up pair
+    (shared T), every row against the oracle."""
+    pr = inputs.lora_problem(M, 4096, 4096, 128, 256.0, block=16, name=f"bnd.q.{M}")
+    assert gemm_err(_gpu_run(pr), _ref(pr)) <= GEMM_TOL
+    prs = [inputs.lora_problem(M, 4096, 14336, 128, 256.0, block=16, name=f"bnd.gu{i}.{M}")
+           for i in range(2)]
+    rows = torch.randperm(M, generator=inputs.generator(f"bnd.rows.{M}"))[:24]
+    for pr, y in zip(prs, _batched(prs)):
+        assert gemm_err(y[rows.cuda()], _ref(pr, rows)) <= GEMM_TOL
+
+
+def test_large_m_deterministic_and_gate_zero_rows():
+    """Data-parallel waves at M = 2048: two calls give the same bits, and
+    gate-0 rows equal a call with every gate 0."""
+    pr = inputs.lora_problem(2048, 4096, 4096, 128, 256.0, block=16, name="det.large")
+    a, b = _gpu_run(pr), _gpu_run(pr)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    pr0 = inputs.LoraProblem(pr.x, pr.W, pr.A, pr.B, torch.zeros_like(pr.gate), pr.alpha)
+    z = (pr.gate == 0).cuda()
+    assert torch.equal(a[z].view(torch.int16), _gpu_run(pr0)[z].view(torch.int16))
 
 
 def test_gate_zero_rows_bit_equal_all_gates_zero():
