@@ -1041,6 +1041,26 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     tl[nt++] = f;
   }
   const int n_down = nt;
+  // Large M: 256-wide output tiles, or 128-wide ones when those fill the
+  // waves of whole tiles better.  A 128-wide tile moves 32 KB of operands
+  // per 128 output columns and K-block against 48 KB per 256, and the
+  // mainloop is bound by that traffic, so its work counts 4/3.
+  int bn_large = 256;
+  if (!P.swap) {
+    auto wave_cost = [&](int bn) {
+      int64_t tiles = 0, work = 0;
+      for (int i = 0; i < n_down; ++i) tiles += tl[i].tiles;
+      for (int p = 0; p < n; ++p) {
+        const int64_t t = ((M + kBM - 1) / kBM) * ((pr[p].d_out + bn - 1) / bn);
+        tiles += t;
+        work += t * ((pr[p].d_in + kBK - 1) / kBK) * bn;
+      }
+      const int64_t G0 = std::min(sms, kMaxGrid);
+      return tiles >= G0 ? ((tiles + G0 - 1) / G0) * G0 * (work / tiles) : INT64_MAX;
+    };
+    const int64_t c128 = wave_cost(128), c256 = wave_cost(256);
+    if (c128 != INT64_MAX && (c256 == INT64_MAX || c128 / 3 * 4 < c256)) bn_large = 128;
+  }
   for (int p = 0; p < n; ++p) {
     Phase f{};
     f.prob = p;
@@ -1053,7 +1073,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
       f.tiles = f.tiles_a;
     } else {
       f.tiles_a = int((M + kBM - 1) / kBM);
-      f.bn = pick_bn(pr[p].d_out);
+      f.bn = std::min(pick_bn(pr[p].d_out), bn_large);
       f.tiles = f.tiles_a * int((pr[p].d_out + f.bn - 1) / f.bn);
     }
     f.tiles_all = f.tiles;
