@@ -867,6 +867,56 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                 store16(P, f, pb, ta, tb, row, c0, v);
               }
             }
+          } else if (sec == kMain) {
+            // Finisher of a wide tile in its CTA's last piece: the CTA's MMAs
+            // are done and its producers finished, so the idle ring stages a
+            // column slice of every contributor's partial per round (bulk
+            // copies), summed in CTA order after the CTA's own accumulator.
+            int nc = 0;
+            for (int c = cta + 1; c <= c1; ++c) nc += P.lo[sec][c] < P.lo[sec][c + 1];
+            int wcols = f.bn;
+            while (wcols > 16 && uint32_t(nc) * uint32_t(wcols) * kBM * 4 > uint32_t(STAGES) * kStage)
+              wcols >>= 1;
+            float* ring = reinterpret_cast<float*>(smem);
+            const float4* ring4 = reinterpret_cast<const float4*>(smem);
+            for (int cw = 0; cw < f.bn; cw += wcols) {
+              if (nc > 0) {
+                if (et == 0) {
+                  fence_proxy_async();
+                  ptx::mbar_arrive_expect_tx(stg_bar, uint32_t(nc) * uint32_t(wcols) * kBM * 4);
+                  int i = 0;
+                  for (int c = cta + 1; c <= c1; ++c) {
+                    if (P.lo[sec][c] == P.lo[sec][c + 1]) continue;
+                    ptx::bulk_load(ring + size_t(i) * wcols * kBM,
+                                   P.partial + (size_t(c) * 2 + sec) * kSlot + size_t(cw) * kBM,
+                                   uint32_t(wcols) * kBM * 4, stg_bar);
+                    ++i;
+                  }
+                }
+                const bool bad = !ptx::mbar_wait(stg_bar, stg_phase & 1, kWaitLimitNs);
+                ++stg_phase;
+                if (epi_sync_or(bad)) {
+                  *abort_flag = 1;
+                  goto done;
+                }
+              }
+              for (int c0 = cw; c0 < cw + wcols; c0 += 16) {
+                float v[16];
+                tmem_ld16f(tq + c0, v);
+                for (int i = 0; i < nc; ++i) {
+#pragma unroll
+                  for (int j4 = 0; j4 < 4; ++j4) {
+                    const float4 t = ring4[(size_t(i) * wcols / 4 + (c0 - cw) / 4 + j4) * kBM + row];
+                    v[4 * j4] += t.x;
+                    v[4 * j4 + 1] += t.y;
+                    v[4 * j4 + 2] += t.z;
+                    v[4 * j4 + 3] += t.w;
+                  }
+                }
+                store16(P, f, pb, ta, tb, row, c0, v);
+              }
+              epi_sync();  // the ring is refilled only once every thread has read it
+            }
           } else {
             // finisher of a wide tile: own accumulator, then the partials of
             // up to four contributors at a time, in CTA order
