@@ -148,7 +148,7 @@ __host__ __device__ constexpr bool pre_merge() {
 }
 template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t staging_bytes() {
-  return pre_merge<BNMAX>() ? (LOCALT ? 32u * 1024 : uint32_t(kSharedTStaging)) : 0u;
+  return pre_merge<BNMAX>() ? (LOCALT ? 64u * 1024 : uint32_t(kSharedTStaging)) : 0u;
 }
 template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr int staging_slots() {  // partials the staging area holds at once
