@@ -1182,15 +1182,39 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     const int64_t slots =
         bnmax <= 64 ? std::max<int64_t>(1, kSharedTStaging / (int64_t(bnmax) * kBM * 4)) : 16;
     int64_t kd = std::max<int64_t>(4, (max_down_nkb + slots - 1) / slots);
+    // a long T tile (down projection of a wide input) may take two rounds:
+    // shorter pieces finish T sooner than one more round of copies costs
+    if (P.swap && kd > 16) kd = (kd + 1) / 2;
     if (!P.swap) kd = std::max<int64_t>(kd, std::min<int64_t>(max_down_nkb, Wt / G / 2));
     Gd = int(std::max<int64_t>(1, std::min<int64_t>(G, (D + kd - 1) / kd)));
   }
   for (int c = 0; c <= G; ++c) P.lo[kDown][c] = c <= Gd && Gd > 0 ? int64_t(c) * D / Gd : D;
   // Main section: CTA c's range ends where the first c+1 CTAs have streamed
-  // (c+1)/G of the section's K-blocks, down ones included.
+  // (c+1)/G of the section's K-blocks, down ones included -- except that a
+  // CTA finishing a split T tile (it waits for and merges the tile's pieces,
+  // then publishes T) takes no main work, which the others share.
+  bool t_fin[kMaxGrid + 1] = {};
+  int n_fin = 0;
+  for (int c = 0; c < G && D > 0; ++c) {
+    const int64_t lo0 = P.lo[kDown][c], hi0 = P.lo[kDown][c + 1];
+    if (lo0 >= hi0) continue;
+    // the CTA's last down piece starts a T tile that continues beyond it
+    int p = P.ph0[kDown];
+    int64_t k = hi0 - 1;
+    while (p + 1 < P.ph1[kDown] && P.ph[p + 1].kb_start <= k) ++p;
+    const Phase& f = P.ph[p];
+    const int64_t ts = f.kb_start + (k - f.kb_start) / f.nkb * f.nkb;
+    if (ts >= lo0 && ts + f.nkb > hi0) {
+      t_fin[c] = true;
+      ++n_fin;
+    }
+  }
+  if (n_fin >= G) n_fin = 0, std::memset(t_fin, 0, sizeof(t_fin));
   P.lo[kMain][0] = 0;
+  int64_t share_before = 0;  // weighted CTAs before c
   for (int c = 1; c < G; ++c) {
-    const int64_t v = int64_t(c) * Wt / G - P.lo[kDown][c];
+    share_before += t_fin[c - 1] ? 0 : 1;
+    const int64_t v = share_before * Wt / (G - n_fin) - P.lo[kDown][c];
     P.lo[kMain][c] = std::min(Mn, std::max(P.lo[kMain][c - 1], v));
   }
   P.lo[kMain][G] = Mn;
