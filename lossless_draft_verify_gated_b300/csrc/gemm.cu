@@ -118,6 +118,7 @@ struct Params {
   int ph0[2], ph1[2];  // stream-K section s holds phases [ph0[s], ph1[s])
   int dp0, dp1;        // data-parallel phases [dp0, dp1) (large M)
   int dp_tiles;        // tiles of the data-parallel waves: tile t goes to CTA t % grid
+  int nprob;           // problems of the launch
   int swap;
   int localt;  // swap path with per-piece adapter
   int M;
@@ -187,11 +188,13 @@ __host__ __device__ constexpr uint32_t tmem_cols() {
 // Barriers and the TMEM slot, then a copy of the kernel parameters.
 constexpr uint32_t kBarrierBytes = 512;
 constexpr uint32_t kParamsBytes = (uint32_t(sizeof(Params)) + 15u) & ~15u;
+// Decode order: the gates of every problem's tokens, staged once per CTA.
+constexpr uint32_t kGateBytes = uint32_t(kMaxLoraProblems) * uint32_t(kSwapMaxRows);
 template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t smem_bytes_for() {
   return uint32_t(stages_for<BNMAX, LOCALT>()) * stage_bytes<BNMAX, LOCALT>() +
          tprime_bytes<BNMAX, LOCALT>() + staging_bytes<BNMAX, LOCALT>() + kBarrierBytes + kParamsBytes +
-         1024;
+         kGateBytes + 1024;
 }
 
 // A piece: K-blocks [s, e) of tile `tile` (whose K-blocks are [tstart, tend)),
@@ -358,7 +361,8 @@ __device__ __forceinline__ bool wait_ready(const Params& P, int sec, int c_from,
 // Stores 16 consecutive accumulator columns (c0 .. c0+15) of TMEM lane `row`.
 // Must be called by all 32 lanes of the warp (the swap path shuffles).
 __device__ __forceinline__ void store16(const Params& P, const Phase& f, const Prob& pb, int ta,
-                                       int tb, int row, int c0, const float (&v)[16]) {
+                                       int tb, int row, int c0, const float (&v)[16],
+                                       const uint8_t* gate_s) {
   const int ncols = f.down ? pb.r : pb.d_out;
   __nv_bfloat16* dst16 = static_cast<__nv_bfloat16*>(f.down ? pb.t : pb.y);
   if (P.swap) {
@@ -386,7 +390,7 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
       const int m = tb * f.bn + c0 + 8 * g + i;  // token of this lane
       if (m >= P.M || n >= ncols) continue;
       if (f.down) {
-        const float gs = float(pb.gate[m]) * pb.scale;
+        const float gs = float(gate_s[f.prob * int(kSwapMaxRows) + m]) * pb.scale;
 #pragma unroll
         for (int j = 0; j < 8; ++j) r[j] *= gs;
       }
@@ -485,6 +489,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     for (uint32_t i = threadIdx.x; i < sizeof(Params) / 4; i += kThreads) dst[i] = src[i];
   }
   const Params& P = *sp;
+  uint8_t* gate_s = reinterpret_cast<uint8_t*>(sp) + kParamsBytes;  // [problem][token] (swap)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -576,22 +581,6 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             const int kl = local_ad ? 0 : int(piece_kb(g, f.na, i) - g.tstart);
             const bool adapter = !LOCALT && kl < f.na;
             if ((it & 1u) != mine) continue;  // the other producer's stage
-            if (adapter && !t_ready_flag) {
-              // The rows of T this tile reads must be complete before TMA reads them.
-              bool ok = true;
-              if (SWAP) {
-                for (int j = 0; j < pb.ttiles && ok; ++j)
-                  ok = wait_flag(P.tflag + pb.tflag0 + j, kWaitLimitNs);
-              } else {
-                ok = wait_flag(P.tflag + pb.tflag0 + ta, kWaitLimitNs);
-              }
-              if (!ok) {
-                *abort_flag = 1;
-                break;
-              }
-              fence_proxy_async();
-              t_ready_flag = true;
-            }
             const int s = int(it % STAGES);
             if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitLimitNs)) {
               *abort_flag = 1;
@@ -622,8 +611,30 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             const bool down_slice = LOCALT && pb.r > 0;
             ptx::mbar_arrive_expect_tx(
                 &full[s], kABytes + uint32_t(f.bn) * kBK * 2 + (down_slice ? kABytes : 0u));
-            ptx::tma_load_2d(sa, ma, &full[s], kc, ta * kBM, polA);
-            ptx::tma_load_2d(sa + kABytes, mb, &full[s], kc, tb * f.bn, polB);
+            // an adapter K-block's weight tile (the up-projection rows) goes out first
+            if (adapter) ptx::tma_load_2d(SWAP ? sa : sa + kABytes, SWAP ? ma : mb, &full[s], kc,
+                                          SWAP ? ta * kBM : tb * f.bn, SWAP ? polA : polB);
+            if (adapter && !t_ready_flag) {
+              // The rows of T this tile reads must be complete before TMA reads
+              // them.  Should the wait give up, T is loaded all the same (the
+              // stage must complete before the CTA may exit) and the launch aborts.
+              bool ok = true;
+              if (SWAP) {
+                for (int j = 0; j < pb.ttiles && ok; ++j)
+                  ok = wait_flag(P.tflag + pb.tflag0 + j, kWaitLimitNs);
+              } else {
+                ok = wait_flag(P.tflag + pb.tflag0 + ta, kWaitLimitNs);
+              }
+              if (!ok) *abort_flag = 1;
+              fence_proxy_async();
+              t_ready_flag = true;
+            }
+            if (!adapter || !SWAP) ptx::tma_load_2d(sa, ma, &full[s], kc, ta * kBM, polA);
+            if (!adapter || SWAP) ptx::tma_load_2d(sa + kABytes, mb, &full[s], kc, tb * f.bn, polB);
+            if (*abort_flag) {
+              ++it;  // this stage's copies are in flight: the exit path waits for them
+              break;
+            }
             if (down_slice) ptx::tma_load_2d(sa + kABytes + kBSlot, &mp[MAP_A], &full[s], kc, 0, polB);
           }
         }
@@ -723,6 +734,12 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     const int et = threadIdx.x - 64;
     uint32_t stg_phase = 0;  // phases of stg_bar used so far
     uint32_t tcount = 0;     // (swap) T drains so far
+    if (SWAP) {
+      // the gates, read where they are needed, are one shared-memory load away
+      for (int p = 0; p < P.nprob; ++p)
+        for (int m = et; m < P.M; m += kEpiThreads) gate_s[p * int(kSwapMaxRows) + m] = P.pb[p].gate[m];
+      epi_sync();
+    }
     int seg = 0;
     PieceIter pit(P, cta);
     Seg g;
@@ -759,7 +776,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int m = c0 + j;
-                const float gs = m < P.M ? float(__ldg(pb.gate + m)) * pb.scale : 0.f;
+                const float gs = m < P.M ? float(gate_s[f.prob * int(kSwapMaxRows) + m]) * pb.scale : 0.f;
                 const __nv_bfloat16 h = __float2bfloat16_rn(v[j] * gs);
                 *reinterpret_cast<__nv_bfloat16*>(tk + m * 128 + ((((jj >> 3) ^ (m & 7))) << 4) +
                                                   (jj & 7) * 2) = h;
@@ -772,8 +789,18 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(t_smem);
         }
+        // A wide tile's finisher in its CTA's last piece merges through the
+        // ring, which is idle once the piece's MMAs are done (no piece
+        // follows it).  Decode-width finishers fetch their partials into the
+        // staging area instead, while their own accumulator is still being
+        // filled: that overlap measured faster, for T tiles too, than one
+        // round through the ring after it.
+        const bool last_piece = sec == kMain || P.lo[kMain][cta] == P.lo[kMain][cta + 1];
+        const bool ring = finisher && last_piece && !kPreMerge;
         float pre[kPreMerge ? BNMAX : 1];
-        if (finisher) {
+        if (ring) {
+          if (et == 0) fail = !wait_ready(P, sec, cta + 1, c1, kWaitLimitNs);
+        } else if (finisher) {
           if constexpr (kPreMerge) {
             // While the tensor cores finish this piece, bring the contributors'
             // partials into shared memory (one bulk copy each) and sum them in
@@ -843,7 +870,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             for (int c0 = 0; c0 < f.bn; c0 += 16) {
               float v[16];
               tmem_ld16f(tq + c0, v);
-              store16(P, f, pb, ta, tb, row, c0, v);
+              store16(P, f, pb, ta, tb, row, c0, v, gate_s);
             }
           } else if (!finisher) {
             // contributor: leave the piece as a partial and raise this CTA's flag
@@ -856,6 +883,62 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                 __stcg(dst + ((c0 >> 2) + i) * kBM + row,
                        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
             }
+          } else if (ring) {
+            // The CTA's MMAs are done and its producers finished, so the idle
+            // ring stages a column slice of as many contributors' partials as
+            // it holds per round (bulk copies), summed in CTA order after the
+            // CTA's own accumulator.
+            constexpr uint32_t kRing = uint32_t(STAGES) * kStage;
+            int nc = 0;
+            for (int c = cta + 1; c <= c1; ++c) nc += P.lo[sec][c] < P.lo[sec][c + 1];
+            int wcols = f.bn;
+            while (wcols > 16 && uint32_t(nc) * uint32_t(wcols) * kBM * 4 > kRing) wcols >>= 1;
+            // contributors per round: all of them unless the slice is 16 wide
+            const int cap = int(kRing / (uint32_t(wcols) * kBM * 4));
+            float* ringf = reinterpret_cast<float*>(smem);
+            const float4* ring4 = reinterpret_cast<const float4*>(smem);
+            for (int cw = 0; cw < f.bn; cw += wcols) {
+              float v[16];
+              for (int b0 = 0; b0 == 0 || b0 < nc; b0 += cap) {
+                const int nb = std::min(cap, nc - b0);
+                if (nb > 0) {
+                  if (et == 0) {
+                    fence_proxy_async();
+                    ptx::mbar_arrive_expect_tx(stg_bar, uint32_t(nb) * uint32_t(wcols) * kBM * 4);
+                    int i = 0, k = 0;
+                    for (int c = cta + 1; c <= c1 && i < nb; ++c) {
+                      if (P.lo[sec][c] == P.lo[sec][c + 1]) continue;
+                      if (k++ < b0) continue;
+                      ptx::bulk_load(ringf + size_t(i) * wcols * kBM,
+                                     P.partial + (size_t(c) * 2 + sec) * kSlot + size_t(cw) * kBM,
+                                     uint32_t(wcols) * kBM * 4, stg_bar);
+                      ++i;
+                    }
+                  }
+                  const bool bad = !ptx::mbar_wait(stg_bar, stg_phase & 1, kWaitLimitNs);
+                  ++stg_phase;
+                  if (epi_sync_or(bad)) {
+                    *abort_flag = 1;
+                    goto done;
+                  }
+                }
+                for (int c0 = cw; c0 < cw + wcols; c0 += 16) {
+                  if (b0 == 0) tmem_ld16f(tq + c0, v);
+                  for (int i = 0; i < nb; ++i) {
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                      const float4 t = ring4[(size_t(i) * wcols / 4 + (c0 - cw) / 4 + j4) * kBM + row];
+                      v[4 * j4] += t.x;
+                      v[4 * j4 + 1] += t.y;
+                      v[4 * j4 + 2] += t.z;
+                      v[4 * j4 + 3] += t.w;
+                    }
+                  }
+                  if (b0 + nb >= nc) store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+                }
+                if (nb > 0) epi_sync();  // the ring is refilled only once every thread has read it
+              }
+            }
           } else if constexpr (kPreMerge) {
 #pragma unroll
             for (int c0 = 0; c0 < BNMAX; c0 += 16) {
@@ -864,58 +947,8 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                 tmem_ld16f(tq + c0, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += pre[c0 + j];
-                store16(P, f, pb, ta, tb, row, c0, v);
+                store16(P, f, pb, ta, tb, row, c0, v, gate_s);
               }
-            }
-          } else if (sec == kMain) {
-            // Finisher of a wide tile in its CTA's last piece: the CTA's MMAs
-            // are done and its producers finished, so the idle ring stages a
-            // column slice of every contributor's partial per round (bulk
-            // copies), summed in CTA order after the CTA's own accumulator.
-            int nc = 0;
-            for (int c = cta + 1; c <= c1; ++c) nc += P.lo[sec][c] < P.lo[sec][c + 1];
-            int wcols = f.bn;
-            while (wcols > 16 && uint32_t(nc) * uint32_t(wcols) * kBM * 4 > uint32_t(STAGES) * kStage)
-              wcols >>= 1;
-            float* ring = reinterpret_cast<float*>(smem);
-            const float4* ring4 = reinterpret_cast<const float4*>(smem);
-            for (int cw = 0; cw < f.bn; cw += wcols) {
-              if (nc > 0) {
-                if (et == 0) {
-                  fence_proxy_async();
-                  ptx::mbar_arrive_expect_tx(stg_bar, uint32_t(nc) * uint32_t(wcols) * kBM * 4);
-                  int i = 0;
-                  for (int c = cta + 1; c <= c1; ++c) {
-                    if (P.lo[sec][c] == P.lo[sec][c + 1]) continue;
-                    ptx::bulk_load(ring + size_t(i) * wcols * kBM,
-                                   P.partial + (size_t(c) * 2 + sec) * kSlot + size_t(cw) * kBM,
-                                   uint32_t(wcols) * kBM * 4, stg_bar);
-                    ++i;
-                  }
-                }
-                const bool bad = !ptx::mbar_wait(stg_bar, stg_phase & 1, kWaitLimitNs);
-                ++stg_phase;
-                if (epi_sync_or(bad)) {
-                  *abort_flag = 1;
-                  goto done;
-                }
-              }
-              for (int c0 = cw; c0 < cw + wcols; c0 += 16) {
-                float v[16];
-                tmem_ld16f(tq + c0, v);
-                for (int i = 0; i < nc; ++i) {
-#pragma unroll
-                  for (int j4 = 0; j4 < 4; ++j4) {
-                    const float4 t = ring4[(size_t(i) * wcols / 4 + (c0 - cw) / 4 + j4) * kBM + row];
-                    v[4 * j4] += t.x;
-                    v[4 * j4 + 1] += t.y;
-                    v[4 * j4 + 2] += t.z;
-                    v[4 * j4 + 3] += t.w;
-                  }
-                }
-                store16(P, f, pb, ta, tb, row, c0, v);
-              }
-              epi_sync();  // the ring is refilled only once every thread has read it
             }
           } else {
             // finisher of a wide tile: own accumulator, then the partials of
@@ -949,7 +982,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                     }
                   }
               }
-              store16(P, f, pb, ta, tb, row, c0, v);
+              store16(P, f, pb, ta, tb, row, c0, v, gate_s);
             }
           }
           // the accumulator may be reused
@@ -1155,6 +1188,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     P.dp1 = nph;
   }
   P.dp_tiles = int(dp_tiles);
+  P.nprob = n;
   // Stream-K sections over the remaining tiles: 0 = T tiles, 1 = y tiles.
   int64_t sec_kb[2] = {0, 0};
   for (int sec = 0; sec < 2; ++sec) {
