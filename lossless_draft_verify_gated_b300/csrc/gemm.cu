@@ -74,9 +74,9 @@ constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 4 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
-constexpr int kPrefetchKBlocks = 8;
+constexpr int kPrefetchKBlocks = 8;  // weight tiles hinted into L2 before the previous launch ends
 constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;
-constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand  // weight tiles hinted into L2 before the previous launch ends
+constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand
 constexpr int kDown = 0, kMain = 1;
 
 enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, kMapsPerProblem = 5 };
