@@ -9,6 +9,7 @@ compiles that C file with gcc and marshals numpy arrays into it.
 Functions (each documented in uno_oracle.c with the passage it follows):
   gated_lora_linear(x, W, A, B, gate, alpha)  -> y (float64)
   verify_block(p_logits, q_logits, draft, u_accept, u_resample)  -> VerifyResult
+  verify_block_ex(..., temperature, mode)  -> VerifyResult (temperature, inverse-CDF resample)
   draft_sample(logits, u)  -> (tokens, status, margin)
 """
 from __future__ import annotations
@@ -53,6 +54,9 @@ def _load():
     lib.oracle_verify_block_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
                                             P, P, P, P, P, P]
     lib.oracle_verify_block_f64.restype = ctypes.c_int
+    lib.oracle_verify_block_ex_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                               ctypes.c_double, ctypes.c_int, P, P, P, P, P, P]
+    lib.oracle_verify_block_ex_f64.restype = ctypes.c_int
     lib.oracle_draft_sample_f64.argtypes = [P, P, I64, I64, P, P, P]
     lib.oracle_draft_sample_f64.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -135,6 +139,38 @@ def verify_block(p_logits, q_logits, draft, u_accept, u_resample) -> VerifyResul
                                      _ptr(st), _ptr(am), _ptr(rm))
     if rc != 0:
         raise RuntimeError(f"oracle_verify_block_f64 failed: {rc}")
+    return VerifyResult(n_acc, toks, n_em, st, am, rm)
+
+
+RESAMPLE_MODES = {"race": 0, "inverse_cdf": 1}
+
+
+def verify_block_ex(p_logits, q_logits, draft, u_accept, u_resample, temperature: float = 1.0,
+                    resample: str = "race") -> VerifyResult:
+    """The verifier at temperature T with the resample drawn by the exponential
+    race (u_resample [Bn, V]) or by the inverse CDF (u_resample [Bn]).  In
+    inverse-CDF mode race_margin holds that sampler's bucket-edge margin."""
+    lib = _load()
+    mode = RESAMPLE_MODES[resample]
+    p = _np(p_logits, np.float32)
+    q = _np(q_logits, np.float32)
+    Bn, Kp, V = p.shape
+    K = q.shape[1]
+    d = _np(draft, np.int32).reshape(Bn, K)
+    ua = _np(u_accept, np.float32).reshape(Bn, K)
+    ur = _np(u_resample, np.float32).reshape(Bn, V) if mode == 0 else \
+        _np(u_resample, np.float32).reshape(Bn)
+    n_acc = np.zeros(Bn, np.int32)
+    toks = np.full((Bn, K + 1), -1, np.int32)
+    n_em = np.zeros(Bn, np.int32)
+    st = np.zeros(Bn, np.int32)
+    am = np.full((Bn, K), np.inf)
+    rm = np.full(Bn, np.inf)
+    rc = lib.oracle_verify_block_ex_f64(_ptr(p), _ptr(q), _ptr(d), _ptr(ua), _ptr(ur),
+                                        Bn, K, Kp, V, float(temperature), mode, _ptr(n_acc),
+                                        _ptr(toks), _ptr(n_em), _ptr(st), _ptr(am), _ptr(rm))
+    if rc != 0:
+        raise RuntimeError(f"oracle_verify_block_ex_f64 failed: {rc}")
     return VerifyResult(n_acc, toks, n_em, st, am, rm)
 
 

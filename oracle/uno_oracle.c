@@ -274,6 +274,161 @@ int oracle_verify_block_f64(const float *p_logits, const float *q_logits,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Sampling variants of the verifier: temperature and a single-uniform      */
+/* inverse-CDF resample.  [Explainer] "The Psi-Spec Sampler": the           */
+/* acceptance rule of speculative decoding, with every distribution taken   */
+/* at sampling temperature T (p = softmax(l_p / T), q = softmax(l_q / T);   */
+/* the drafts are assumed drawn from q at the same T).                      */
+/* ------------------------------------------------------------------------ */
+static int softmax_row_temp_f64(const float *logits, int64_t V, double T, double *prob)
+{
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        const double raw = (double)logits[v];
+        if (isnan(raw) || (isinf(raw) && raw > 0)) return 1;
+        const double l = raw / T;
+        if (l > m) m = l;
+    }
+    if (isinf(m)) return 1;
+    double z = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        prob[v] = exp((double)logits[v] / T - m);
+        z += prob[v];
+    }
+    for (int64_t v = 0; v < V; ++v) prob[v] /= z;
+    return 0;
+}
+
+/* Inverse CDF with one uniform u in [0,1): the smallest v whose cumulative
+ * weight C(v) = w[0] + ... + w[v] exceeds u * S, S = C(V-1); the vocabulary
+ * order is the order of the CDF.  *margin receives the distance from u*S to
+ * the nearer edge of the chosen bucket, relative to S. */
+static int32_t inv_cdf_f64(const double *w, double u, int64_t V, double *margin)
+{
+    double S = 0.0;
+    for (int64_t v = 0; v < V; ++v) S += w[v];
+    const double t = u * S;
+    double c = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        const double prev = c;
+        c += w[v];
+        if (c > t) {
+            if (margin) *margin = fmin(c - t, t - prev) / S;
+            return (int32_t)v;
+        }
+    }
+    for (int64_t v = V - 1; v >= 0; --v)
+        if (w[v] > 0.0) {
+            if (margin) *margin = 0.0;
+            return (int32_t)v;
+        }
+    return -1;
+}
+
+/* As oracle_verify_block_f64, at temperature T > 0, with the resample drawn
+ * by mode 0 (exponential race, u_res [Bn,V]) or mode 1 (inverse CDF, u_res
+ * [Bn], one uniform in [0,1) per sequence).  race_margin receives the race's
+ * margin or, in mode 1, the inverse CDF's. */
+int oracle_verify_block_ex_f64(const float *p_logits, const float *q_logits,
+                               const int32_t *draft, const float *u_acc,
+                               const float *u_res, int64_t Bn, int64_t K,
+                               int64_t Kp, int64_t V, double T, int mode,
+                               int32_t *n_accepted, int32_t *out_tokens,
+                               int32_t *n_emitted, int32_t *status,
+                               double *accept_margin, double *race_margin)
+{
+    if (Bn < 0 || K < 0 || V <= 0 || (Kp != K && Kp != K + 1)) return OR_ERR_ARG;
+    if (!(T > 0.0) || isinf(T) || (mode != 0 && mode != 1)) return OR_ERR_ARG;
+    if (Bn == 0) return OR_OK;
+    if (!p_logits || (K > 0 && (!q_logits || !draft || !u_acc)) || !u_res ||
+        !n_accepted || !out_tokens || !n_emitted || !status)
+        return OR_ERR_ARG;
+    int err = OR_OK;
+
+#pragma omp parallel
+    {
+        double *P = (double *)malloc(sizeof(double) * (size_t)(Kp > 0 ? Kp : 1) * (size_t)V);
+        double *Q = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)V);
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!P || !Q || !r) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t b = 0; b < Bn; ++b) {
+            if (!P || !Q || !r) continue;
+            int32_t *out = out_tokens + b * (K + 1);
+            for (int64_t i = 0; i <= K; ++i) out[i] = -1;
+            if (accept_margin)
+                for (int64_t i = 0; i < K; ++i) accept_margin[b * K + i] = INFINITY;
+            if (race_margin) race_margin[b] = INFINITY;
+            n_accepted[b] = 0;
+            n_emitted[b] = 0;
+            status[b] = OR_SEQ_OK;
+
+            for (int64_t i = 0; i < K; ++i) {
+                const int32_t x = draft[b * K + i];
+                if (x < 0 || x >= V) status[b] = OR_SEQ_BAD_DRAFT;
+            }
+            /* Step 1: softmax of every row at temperature T. */
+            int bad = 0;
+            for (int64_t i = 0; i < Kp; ++i)
+                bad |= softmax_row_temp_f64(p_logits + (b * Kp + i) * V, V, T, P + i * V);
+            for (int64_t i = 0; i < K; ++i)
+                bad |= softmax_row_temp_f64(q_logits + (b * K + i) * V, V, T, Q + i * V);
+            if (bad && status[b] == OR_SEQ_OK) status[b] = OR_SEQ_NONFINITE;
+            if (status[b] != OR_SEQ_OK) continue;
+
+            /* Step 2: the acceptance rule, unchanged. */
+            int64_t n = 0;
+            for (int64_t i = 0; i < K; ++i) {
+                const int32_t x = draft[b * K + i];
+                const double pi = P[i * V + x];
+                const double qi = Q[i * V + x];
+                const double rho = qi > 0.0 ? pi / qi : INFINITY;
+                const double thr = rho < 1.0 ? rho : 1.0;
+                const double u = (double)u_acc[b * K + i];
+                if (accept_margin) accept_margin[b * K + i] = fabs(thr - u);
+                if (u < thr) {
+                    out[i] = x;
+                    ++n;
+                } else {
+                    break;
+                }
+            }
+            n_accepted[b] = (int32_t)n;
+            n_emitted[b] = (int32_t)n;
+
+            /* Step 3: the residual (or bonus) token, by the chosen sampler. */
+            double *rm = race_margin ? race_margin + b : NULL;
+            const double *w = NULL;
+            if (n < K) {
+                double S = 0.0;
+                for (int64_t v = 0; v < V; ++v) {
+                    const double d = P[n * V + v] - Q[n * V + v];
+                    r[v] = d > 0.0 ? d : 0.0;
+                    S += r[v];
+                }
+                if (S == 0.0)
+                    for (int64_t v = 0; v < V; ++v) r[v] = P[n * V + v];
+                w = r;
+            } else if (Kp == K + 1) {
+                w = P + K * V;
+            }
+            if (w) {
+                out[n] = mode == 0 ? race_f64(w, u_res + b * V, V, rm)
+                                   : inv_cdf_f64(w, (double)u_res[b], V, rm);
+                n_emitted[b] = (int32_t)(n + 1);
+            }
+        }
+        free(P);
+        free(Q);
+        free(r);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Draft sampling (Psi-Spec linear sampler, drafting half).                 */
 /* [Explainer] "The Psi-Spec Sampler": the linear sampler draws one         */
 /* candidate per token position.  tokens[r] = argmax_v q_r(v) / (-ln u[r,v])*/
