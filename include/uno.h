@@ -195,6 +195,36 @@ int uno_verify_block(const float *p_logits, const float *q_logits,
                      void *workspace, size_t ws_bytes, uno_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Block verifier with sampling variants: temperature and the resample draw.
+ * (Same rule and passages as uno_verify_block; the pages sample at
+ * temperature 1 and say only that the residual is resampled.)
+ *   temperature  T > 0, finite: every distribution is taken at T,
+ *                p_i = softmax(p_logits[b,i,:] / T), q_i likewise (the drafts
+ *                are expected to come from q at the same T).  T == 1 with
+ *                UNO_RESAMPLE_RACE gives exactly uno_verify_block's outputs.
+ *   resample     UNO_RESAMPLE_RACE: the exponential race of uno_verify_block,
+ *                u_resample [Bn, V] float32 in (0,1);
+ *                UNO_RESAMPLE_INVERSE_CDF: one uniform per sequence,
+ *                u_resample [Bn] float32 in [0,1); the token is the smallest v
+ *                whose cumulative weight (vocabulary order) exceeds u * S,
+ *                S the weights' sum, with the weights summed in fp64.  Its
+ *                result agrees with an fp64 evaluation except when u * S falls
+ *                within rounding of a bucket edge.
+ * Other arguments, outputs, workspace and requirements as uno_verify_block;
+ * UNO_ERR_ARG for a temperature that is not finite and positive or an
+ * unknown mode.
+ * ------------------------------------------------------------------------- */
+enum { UNO_RESAMPLE_RACE = 0, UNO_RESAMPLE_INVERSE_CDF = 1 };
+
+int uno_verify_block_ex(const float *p_logits, const float *q_logits,
+                        const int32_t *draft, const float *u_accept,
+                        const float *u_resample, int64_t Bn, int64_t K,
+                        int64_t Kp, int64_t V, float temperature, int resample,
+                        int32_t *n_accepted, int32_t *out_tokens,
+                        int32_t *n_emitted, int32_t *status, void *workspace,
+                        size_t ws_bytes, uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Block verifier that allocates nothing (the paper has no counterpart: this is
  * a library convenience).  For callers that cannot provide device scratch --
  * e.g. an op embedded in another runtime that receives only its input and

@@ -40,6 +40,8 @@ SIGNATURES = {
     "uno_verify_block": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ,
                               _P]),
     "uno_draft_sample": (_I, [_P, _P, _I64, _I64, _P, _P, _P]),
+    "uno_verify_block_ex": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float, _I,
+                                 _P, _P, _P, _P, _P, _SZ, _P]),
     "uno_verify_block_no_alloc_max_scratch": (_SZ, []),
     "uno_verify_block_no_alloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                        _P]),
@@ -198,6 +200,35 @@ def uno_verify_block(p_logits, q_logits, draft, u_accept, u_resample, *, out=Non
                                 _dptr(n_em), _dptr(st), _dptr(workspace), workspace.numel(),
                                 _stream(stream))
     _check("uno_verify_block", rc)
+    return n_acc, toks, n_em, st
+
+
+UNO_RESAMPLE_RACE = 0
+UNO_RESAMPLE_INVERSE_CDF = 1
+_RESAMPLE = {"race": UNO_RESAMPLE_RACE, "inverse_cdf": UNO_RESAMPLE_INVERSE_CDF}
+
+
+def uno_verify_block_ex(p_logits, q_logits, draft, u_accept, u_resample, *, temperature=1.0,
+                        resample="race", out=None, workspace=None, stream=None):
+    """The verifier at `temperature`, resampling by "race" (u_resample [Bn, V])
+    or "inverse_cdf" (u_resample [Bn]).  Returns (n_accepted, out_tokens,
+    n_emitted, status), int32."""
+    Bn, Kp, V = p_logits.shape
+    K = q_logits.shape[1]
+    dev = p_logits.device
+    if out is None:
+        out = (torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty((Bn, K + 1), dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev))
+    n_acc, toks, n_em, st = out
+    if workspace is None:
+        workspace = _workspace(uno_verify_block_workspace(Bn, K, Kp, V), dev)
+    rc = lib().uno_verify_block_ex(_dptr(p_logits), _dptr(q_logits), _dptr(draft), _dptr(u_accept),
+                                   _dptr(u_resample), Bn, K, Kp, V, float(temperature),
+                                   _RESAMPLE[resample], _dptr(n_acc), _dptr(toks), _dptr(n_em),
+                                   _dptr(st), _dptr(workspace), workspace.numel(), _stream(stream))
+    _check("uno_verify_block_ex", rc)
     return n_acc, toks, n_em, st
 
 

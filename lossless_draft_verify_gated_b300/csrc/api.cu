@@ -158,6 +158,32 @@ int uno_verify_block(const float* p_logits, const float* q_logits, const int32_t
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
 
+int uno_verify_block_ex(const float* p_logits, const float* q_logits, const int32_t* draft,
+                        const float* u_accept, const float* u_resample, int64_t Bn, int64_t K,
+                        int64_t Kp, int64_t V, float temperature, int resample,
+                        int32_t* n_accepted, int32_t* out_tokens, int32_t* n_emitted,
+                        int32_t* status, void* workspace, size_t ws_bytes, uno_stream_t stream) {
+  if (!(temperature > 0.0f) || !(temperature < INFINITY)) return UNO_ERR_ARG;
+  if (resample != UNO_RESAMPLE_RACE && resample != UNO_RESAMPLE_INVERSE_CDF) return UNO_ERR_ARG;
+  if (!verify_shape_ok(Bn, K, Kp, V)) return UNO_ERR_ARG;
+  if (Bn == 0) return UNO_OK;
+  if (!p_logits || !u_resample || !n_accepted || !out_tokens || !n_emitted || !status || !workspace)
+    return UNO_ERR_ARG;
+  if (K > 0 && (!q_logits || !draft || !u_accept)) return UNO_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits) |
+       reinterpret_cast<uintptr_t>(u_resample) | reinterpret_cast<uintptr_t>(u_accept)) & 3u)
+    return UNO_ERR_ALIGN;
+  if (!aligned256(workspace)) return UNO_ERR_WORKSPACE;
+  const VerifyPlan pl = plan_verify(Bn, K, Kp, V, sm_count());
+  if (ws_bytes < pl.bytes) return UNO_ERR_WORKSPACE;
+  // logits are scaled by 1/T in fp32 (exact for T == 1)
+  const float inv_t = temperature == 1.0f ? 1.0f : 1.0f / temperature;
+  const cudaError_t e = launch_verify(p_logits, q_logits, draft, u_accept, u_resample, Bn, K, Kp, V,
+                                      n_accepted, out_tokens, n_emitted, status, workspace, pl,
+                                      reinterpret_cast<cudaStream_t>(stream), inv_t, resample);
+  return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
+}
+
 int uno_draft_sample(const float* logits, const float* u, int64_t R, int64_t V, int32_t* tokens,
                      int32_t* status, uno_stream_t stream) {
   if (R < 0 || V < 1 || V >= (int64_t(1) << 31) || R >= (int64_t(1) << 31)) return UNO_ERR_ARG;

@@ -33,7 +33,8 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                           const float* u_acc, const float* u_res, int64_t Bn,
                           int64_t K, int64_t Kp, int64_t V, int32_t* n_acc,
                           int32_t* out_tokens, int32_t* n_emit, int32_t* status,
-                          void* ws, const VerifyPlan& plan, cudaStream_t st);
+                          void* ws, const VerifyPlan& plan, cudaStream_t st,
+                          float inv_t = 1.0f, int mode = 0);  // 1/temperature, UNO_RESAMPLE_*
 
 cudaError_t launch_draft_sample(const float* logits, const float* u, int64_t R,
                                 int64_t V, int32_t* tokens, int32_t* status,

@@ -41,6 +41,7 @@ __device__ __forceinline__ void grid_launch_dependents() {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;  // float4 loads in flight per thread in the statistics pass
+constexpr int kRace = 0, kInverseCdf = 1;  // resample modes (uno.h: UNO_RESAMPLE_*)
 
 struct MS {
   float m, s;  // running max and sum of exp(x - m)
@@ -86,10 +87,12 @@ __device__ __forceinline__ const float* row_ptr(const float* p, const float* q, 
   return j < Kp ? p + (b * Kp + j) * V : q + (b * K + (j - Kp)) * V;
 }
 
+// kEx: logits at a temperature other than 1 (the plain kernel is kept as it was)
+template <bool kEx>
 __global__ void __launch_bounds__(kThreads)
 verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
                     const int32_t* __restrict__ draft, int64_t K, int64_t Kp, int64_t V,
-                    int splits, int64_t chunk, float2* __restrict__ part,
+                    int splits, int64_t chunk, float inv_t, float2* __restrict__ part,
                     float* __restrict__ gathered, int* __restrict__ counter) {
   const int64_t unit = blockIdx.x;
   const int64_t row = unit / splits;
@@ -122,12 +125,12 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const int tid = threadIdx.x;
   if (tid < va - v0) {
     const float x = r[v0 + tid];
-    ms_add1(acc, x);
+    ms_add1(acc, kEx ? x * inv_t : x);
     if (v0 + tid == xd) gathered[row] = x;
   }
   if (tid < v1 - vb) {
     const float x = r[vb + tid];
-    ms_add1(acc, x);
+    ms_add1(acc, kEx ? x * inv_t : x);
     if (vb + tid == xd) gathered[row] = x;
   }
   const float4* vp = reinterpret_cast<const float4*>(r + va);
@@ -143,7 +146,10 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      ms_add4(acc, t[u].x, t[u].y, t[u].z, t[u].w);
+      if (kEx)
+        ms_add4(acc, t[u].x * inv_t, t[u].y * inv_t, t[u].z * inv_t, t[u].w * inv_t);
+      else
+        ms_add4(acc, t[u].x, t[u].y, t[u].z, t[u].w);
       if (xq == i + u * kThreads) {
         const int c = int((xd - va) & 3);
         gathered[row] = c == 0 ? t[u].x : c == 1 ? t[u].y : c == 2 ? t[u].z : t[u].w;
@@ -187,14 +193,18 @@ struct RacePart {
   float sp;  // best score of the AR row itself (fallback and bonus race)
   int vp;
 };
+// (inverse CDF) the same slot holds the chunk's residual and AR weight sums
+static_assert(sizeof(RacePart) == sizeof(double2), "chunk sums share the race slot");
 
 constexpr int kMaxRows = 2 * 256 + 1;  // Kp + K rows of one sequence held in smem
 
+// kEx: temperature other than 1 or the inverse-CDF resample
+template <bool kEx>
 __global__ void __launch_bounds__(kThreads)
 verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
                      const int32_t* __restrict__ draft, const float* __restrict__ u_acc,
                      const float* __restrict__ u_res, int64_t K, int64_t Kp, int64_t V,
-                     int splits, int race_splits, int64_t race_chunk,
+                     int splits, int race_splits, int64_t race_chunk, float inv_t, int mode,
                      const float2* __restrict__ part, const float* __restrict__ gathered,
                      RacePart* __restrict__ rpart,
                      int* __restrict__ counter, int32_t* __restrict__ n_acc,
@@ -219,14 +229,14 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const bool has_i = tid < K;
   const int32_t x_t = has_i ? draft[b * K + tid] : 0;
   const float ua_t = has_i ? u_acc[b * K + tid] : 0.f;
-  const float* ub = u_res + b * V;
+  const float* ub = u_res + b * V;  // (race) this sequence's uniforms
   const int64_t v0 = int64_t(split) * race_chunk;
   const int64_t v1 = min(V, v0 + race_chunk);
   float u_pre[kRaceUnroll];
 #pragma unroll
   for (int i = 0; i < kRaceUnroll; ++i) {
     const int64_t vi = v0 + tid + int64_t(i) * kThreads;
-    u_pre[i] = vi < v1 ? ub[vi] : 0.5f;
+    u_pre[i] = ((!kEx || mode == kRace) && vi < v1) ? ub[vi] : 0.5f;
   }
   if (tid == 0) s_bad = 0;
   grid_dependency_wait();  // the statistics pass's partials, gathered logits and counters
@@ -300,7 +310,8 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       accept = true;  // q_i(x) = 0: ratio +inf
     } else {
       const float lp = gathered[b * per_seq + i];
-      const float lr = (lp - s_lz[i]) - (lq - s_lz[Kp + i]);
+      const float lr = kEx ? (lp * inv_t - s_lz[i]) - (lq * inv_t - s_lz[Kp + i])
+                           : (lp - s_lz[i]) - (lq - s_lz[Kp + i]);
       const float thr = fminf(1.0f, expf(lr));
       accept = ua_t < thr;
     }
@@ -335,6 +346,147 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   // cross-multiplication (den = -ln u > 0), dividing once at the end;
   // probabilities come from exp2 of the scaled, max-shifted logit.
   constexpr float kLog2e = 1.4426950408889634f;
+  if constexpr (kEx) if (mode == kInverseCdf) {
+    __shared__ double s_d[2][kWarps];  // per-warp sums
+    __shared__ long long s_pick;       // chosen chunk, then chosen token
+    __shared__ double s_base;          // weight before the chosen chunk
+    __shared__ double s_loc[2][kThreads];
+    // 3'. Inverse CDF with one uniform u: the token is the smallest v whose
+    //     cumulative weight exceeds u * S, in vocabulary order; weights
+    //     max(0, p_n - q_n) (p_n should those sum to 0), or p_K for the bonus
+    //     token.  Sums in fp64: this CTA's chunk first; the last CTA to arrive
+    //     scans the chunk sums in chunk order, then searches the chunk holding
+    //     the crossing.  Prefix sums are sequential over per-thread partials,
+    //     so consecutive threads' ranges meet exactly and one entry crosses.
+    auto w_p = [&](int64_t v) { return exp2f((pr[v] * inv_t - mp) * kLog2e) * izp; };
+    auto w_r = [&](int64_t v) {
+      const float rv = w_p(v) - exp2f((qr[v] * inv_t - mq) * kLog2e) * izq;
+      return rv > 0.f ? rv : 0.f;
+    };
+    double sr = 0.0, sp = 0.0;
+    for (int64_t v = v0 + tid; v < v1; v += kThreads) {
+      sp += double(w_p(v));
+      if (residual) sr += double(w_r(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sr += __shfl_xor_sync(0xffffffffu, sr, o);
+      sp += __shfl_xor_sync(0xffffffffu, sp, o);
+    }
+    if ((tid & 31) == 0) {
+      s_d[0][tid >> 5] = sr;
+      s_d[1][tid >> 5] = sp;
+    }
+    __syncthreads();
+    double2* csum = reinterpret_cast<double2*>(rpart) + b * race_splits;
+    if (tid == 0) {
+      double a = 0.0, c = 0.0;
+      for (int w = 0; w < kWarps; ++w) {
+        a += s_d[0][w];
+        c += s_d[1][w];
+      }
+      csum[split] = make_double2(a, c);
+      __threadfence();
+      s_last = atomicAdd(&counter[b], 1) == race_splits - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // (a) the chunk holding the crossing
+    const int per = (race_splits + kThreads - 1) / kThreads;
+    const int c_lo = min(race_splits, tid * per), c_hi = min(race_splits, c_lo + per);
+    double lr = 0.0, lpp = 0.0;
+    for (int c = c_lo; c < c_hi; ++c) {
+      const double2 t = __ldcg(csum + c);
+      lr += t.x;
+      lpp += t.y;
+    }
+    s_loc[0][tid] = lr;
+    s_loc[1][tid] = lpp;
+    __syncthreads();
+    if (tid == 0) {
+      double a = 0.0, c = 0.0;
+      for (int t = 0; t < kThreads; ++t) {
+        const double x = s_loc[0][t], y = s_loc[1][t];
+        s_loc[0][t] = a;
+        s_loc[1][t] = c;
+        a += x;
+        c += y;
+      }
+      s_d[0][0] = a;
+      s_d[1][0] = c;
+      s_pick = -1;
+    }
+    __syncthreads();
+    const bool use_r = residual && s_d[0][0] > 0.0;
+    const double S = use_r ? s_d[0][0] : s_d[1][0];
+    const double target = double(u_res[b]) * S;
+    {
+      const double E = s_loc[use_r ? 0 : 1][tid];
+      double loc = 0.0;
+      for (int c = c_lo; c < c_hi; ++c) {
+        const double2 t = __ldcg(csum + c);
+        const double before = E + loc;
+        loc += use_r ? t.x : t.y;
+        if (before <= target && target < E + loc) {
+          s_pick = c;
+          s_base = before;
+        }
+      }
+    }
+    __syncthreads();
+    int64_t tok = -1;
+    if (s_pick >= 0) {
+      // (b) the entry of that chunk where the cumulative weight crosses u * S
+      const int64_t cv0 = s_pick * race_chunk, cv1 = min(V, cv0 + race_chunk);
+      const double base = s_base;
+      const int64_t per2 = (cv1 - cv0 + kThreads - 1) / kThreads;
+      const int64_t e_lo = min(cv1, cv0 + tid * per2), e_hi = min(cv1, e_lo + per2);
+      double l = 0.0;
+      for (int64_t v = e_lo; v < e_hi; ++v) l += double(use_r ? w_r(v) : w_p(v));
+      __syncthreads();
+      s_loc[0][tid] = l;
+      __syncthreads();
+      if (tid == 0) {
+        double a = 0.0;
+        for (int t = 0; t < kThreads; ++t) {
+          const double x = s_loc[0][t];
+          s_loc[0][t] = a;
+          a += x;
+        }
+        s_pick = -1;
+      }
+      __syncthreads();
+      const double E = s_loc[0][tid];
+      double loc = 0.0;
+      int64_t last_pos = -1;
+      for (int64_t v = e_lo; v < e_hi; ++v) {
+        const double wv = double(use_r ? w_r(v) : w_p(v));
+        const double before = base + (E + loc);
+        loc += wv;
+        if (wv > 0.0) last_pos = v;
+        if (before <= target && target < base + (E + loc)) s_pick = v;
+      }
+      s_loc[1][tid] = double(last_pos);
+      __syncthreads();
+      tok = s_pick;
+      if (tok < 0) {
+        // rounding left the crossing just past this chunk's recomputed sum:
+        // its last entry with positive weight
+        for (int t = kThreads - 1; t >= 0 && tok < 0; --t)
+          if (s_loc[1][t] >= 0.0) tok = int64_t(s_loc[1][t]);
+      }
+    }
+    if (tid == 0) {
+      counter[b] = 0;
+      n_acc[b] = n;
+      n_emit[b] = n + 1;
+      status[b] = UNO_SEQ_OK;
+    }
+    for (int64_t i = tid; i <= K; i += kThreads)
+      out[i] = i < n ? x_t : (i == n ? int32_t(tok) : -1);
+    return;
+  }
   float pn = -1.f, pd = 1.f, rn = 0.f, rd = 1.f;
   int pvid = -1, rvid = -1;
   for (int64_t v = v0 + tid; v < v1; v += int64_t(kThreads) * kRaceUnroll) {
@@ -353,14 +505,14 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       const int64_t vi = v + int64_t(i) * kThreads;
       if (vi >= v1) break;
       const float e = -logf(uu[i]);
-      const float pv = exp2f((lp[i] - mp) * kLog2e) * izp;
+      const float pv = exp2f(((kEx ? lp[i] * inv_t : lp[i]) - mp) * kLog2e) * izp;
       if (pv * pd > pn * e) {  // pv / e > pn / pd; ties keep the lower id
         pn = pv;
         pd = e;
         pvid = int(vi);
       }
       if (residual) {
-        const float rv = pv - exp2f((lq[i] - mq) * kLog2e) * izq;
+        const float rv = pv - exp2f(((kEx ? lq[i] * inv_t : lq[i]) - mq) * kLog2e) * izq;
         if (rv > 0.f && rv * rd > rn * e) {
           rn = rv;
           rd = e;
@@ -504,21 +656,31 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                           const float* u_acc, const float* u_res, int64_t Bn, int64_t K,
                           int64_t Kp, int64_t V, int32_t* n_acc, int32_t* out_tokens,
                           int32_t* n_emit, int32_t* status, void* ws, const VerifyPlan& pl,
-                          cudaStream_t st) {
+                          cudaStream_t st, float inv_t, int mode) {
   char* w = static_cast<char*>(ws);
   float2* part = reinterpret_cast<float2*>(w + pl.off_stats);
   float* gathered = reinterpret_cast<float*>(w + pl.off_gather);
   RacePart* rpart = reinterpret_cast<RacePart*>(w + pl.off_race);
   int* counter = reinterpret_cast<int*>(w + pl.off_count);
   const int64_t g1 = pl.rows * pl.splits;
-  verify_stats_kernel<<<dim3(unsigned(g1)), kThreads, 0, st>>>(p, q, draft, K, Kp, V, pl.splits,
-                                                                pl.chunk, part, gathered, counter);
+  const bool ex = inv_t != 1.0f || mode != kRace;
+  if (ex)
+    verify_stats_kernel<true><<<dim3(unsigned(g1)), kThreads, 0, st>>>(
+        p, q, draft, K, Kp, V, pl.splits, pl.chunk, inv_t, part, gathered, counter);
+  else
+    verify_stats_kernel<false><<<dim3(unsigned(g1)), kThreads, 0, st>>>(
+        p, q, draft, K, Kp, V, pl.splits, pl.chunk, inv_t, part, gathered, counter);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t g2 = Bn * pl.race_splits;
-  verify_finish_kernel<<<dim3(unsigned(g2)), kThreads, 0, st>>>(
-      p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, part,
-      gathered, rpart, counter, n_acc, out_tokens, n_emit, status);
+  if (ex)
+    verify_finish_kernel<true><<<dim3(unsigned(g2)), kThreads, 0, st>>>(
+        p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
+        part, gathered, rpart, counter, n_acc, out_tokens, n_emit, status);
+  else
+    verify_finish_kernel<false><<<dim3(unsigned(g2)), kThreads, 0, st>>>(
+        p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
+        part, gathered, rpart, counter, n_acc, out_tokens, n_emit, status);
   return cudaGetLastError();
 }
 
