@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch ops eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--temperature", type=float, default=1.0,
+                    help="sampling temperature of the verifier (drafts drawn from q at the same T)")
+    ap.add_argument("--resample", choices=["race", "inverse_cdf"], default="race",
+                    help="residual/bonus draw: exponential race (default) or single-uniform inverse CDF")
     ap.add_argument("--grouping", choices=["layer", "all", "single"], default="layer",
                     help="layer: [q,k,v] [o] [gate,up] [down], one persistent launch each (the "
                          "layer's data dependencies); all: the 7 projections in one launch; "
@@ -108,8 +112,11 @@ def proj_bytes_flops(M, n_gate1):
     return by, fl
 
 
-def verify_bytes(batch, n_race):
-    return 8 * batch * BLOCK * VOCAB + 12 * batch * BLOCK + 4 * VOCAB * n_race
+def verify_bytes(batch, n_race, resample="race"):
+    """p and q once, drafts and accept uniforms, and the resample's uniforms:
+    a vocabulary row per race, one value per sequence for the inverse CDF."""
+    u = 4 * VOCAB * n_race if resample == "race" else 4 * batch
+    return 8 * batch * BLOCK * VOCAB + 12 * batch * BLOCK + u
 
 
 class Clocks:
@@ -180,7 +187,7 @@ GROUPINGS = {"layer": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
 class Step:
     """All inputs, outputs and workspaces of one step, resident on the device."""
 
-    def __init__(self, batch, sigma, device, grouping="layer"):
+    def __init__(self, batch, sigma, device, grouping="layer", temperature=1.0, resample="race"):
         import torch
         from lossless_draft_verify_gated_b300 import binding, inputs
         self.batch, self.device = batch, device
@@ -199,8 +206,15 @@ class Step:
             self.groups.append((probs, ws))
         vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=device)
         self.p, self.q, self.ua, self.ur = vp.p_logits, vp.q_logits, vp.u_accept, vp.u_resample
-        # drafts: the linear sampler's drafting half, a single token drawn from q at each position
-        self.draft, st = binding.uno_draft_sample(self.q, vp.u_draft)
+        self.temperature, self.resample = temperature, resample
+        self.plain = temperature == 1.0 and resample == "race"
+        if resample == "inverse_cdf":  # one uniform per sequence
+            self.ur = inputs.uniform_accept((batch,), f"verify.u1.B{batch}", device=device)
+        # drafts: the linear sampler's drafting half, a single token drawn from q (at the
+        # verifier's temperature) at each position
+        qd = self.q if temperature == 1.0 else (self.q.double() / temperature).float()
+        self.draft, st = binding.uno_draft_sample(qd, vp.u_draft)
+        del qd
         assert int(st.abs().sum()) == 0
         del vp
         self.vout = tuple(torch.empty(s, dtype=torch.int32, device=device)
@@ -219,8 +233,13 @@ class Step:
 
     def verify(self):
         from lossless_draft_verify_gated_b300 import binding
-        binding.uno_verify_block(self.p, self.q, self.draft, self.ua, self.ur, out=self.vout,
-                                 workspace=self.vws)
+        if self.plain:
+            binding.uno_verify_block(self.p, self.q, self.draft, self.ua, self.ur, out=self.vout,
+                                     workspace=self.vws)
+        else:
+            binding.uno_verify_block_ex(self.p, self.q, self.draft, self.ua, self.ur,
+                                        temperature=self.temperature, resample=self.resample,
+                                        out=self.vout, workspace=self.vws)
 
 
 def run_uno(args):
@@ -230,7 +249,7 @@ def run_uno(args):
     from lossless_draft_verify_gated_b300 import binding
     binding.lib()
     hbm, tflops, tflops_sustained, peak_kind = peaks()
-    st = Step(args.batch, args.sigma, dev, args.grouping)
+    st = Step(args.batch, args.sigma, dev, args.grouping, args.temperature, args.resample)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
 
     # CUDA graphs of the two halves of the step (launch overhead off the clock)
@@ -304,7 +323,7 @@ def run_uno(args):
     else:
         achieved, peak, unit = fl / (ms_proj / 1e3) / 1e12, tflops, "TFLOP/s"
     n_race = int((n_acc < BLOCK).sum())
-    vb = verify_bytes(args.batch, n_race)
+    vb = verify_bytes(args.batch, n_race, args.resample)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
@@ -315,6 +334,7 @@ def run_uno(args):
                    "l2": "flushed before every step (2x L2 write, outside the timed events)",
                    "launch": "CUDA graph per half-step" if g_proj is not None else "eager",
                    "grouping": args.grouping + ": " + " | ".join(",".join(g) for g in GROUPINGS[args.grouping]),
+                   "sampler": f"temperature {args.temperature}, {args.resample} resample",
                    "parallelism": f"dp{ws} (independent replicas, no collective)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4),
@@ -338,7 +358,10 @@ def run_uno(args):
     if not args.no_e2e:
         out["e2e"] = e2e(st, dev, max(5, min(K, 50)))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(st, args.batch, args.sigma, budget_s=15.0)
+        if st.plain:
+            out["cpu_baseline"] = cpu_baseline(st, args.batch, args.sigma, budget_s=15.0)
+        else:  # the timed oracle step is the default sampler's
+            out["cpu_baseline"] = None
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:

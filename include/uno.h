@@ -207,9 +207,10 @@ int uno_verify_block(const float *p_logits, const float *q_logits,
  *                UNO_RESAMPLE_INVERSE_CDF: one uniform per sequence,
  *                u_resample [Bn] float32 in [0,1); the token is the smallest v
  *                whose cumulative weight (vocabulary order) exceeds u * S,
- *                S the weights' sum, with the weights summed in fp64.  Its
- *                result agrees with an fp64 evaluation except when u * S falls
- *                within rounding of a bucket edge.
+ *                S the weights' sum; fp32 weights are summed exactly in
+ *                integer units of 2^-46.  Its result agrees with an fp64
+ *                evaluation except when u * S falls within rounding of a
+ *                bucket edge.
  * Other arguments, outputs, workspace and requirements as uno_verify_block;
  * UNO_ERR_ARG for a temperature that is not finite and positive or an
  * unknown mode.

@@ -194,7 +194,7 @@ struct RacePart {
   int vp;
 };
 // (inverse CDF) the same slot holds the chunk's residual and AR weight sums
-static_assert(sizeof(RacePart) == sizeof(double2), "chunk sums share the race slot");
+static_assert(sizeof(RacePart) == sizeof(longlong2), "chunk sums share the race slot");
 
 constexpr int kMaxRows = 2 * 256 + 1;  // Kp + K rows of one sequence held in smem
 
@@ -347,26 +347,30 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   // probabilities come from exp2 of the scaled, max-shifted logit.
   constexpr float kLog2e = 1.4426950408889634f;
   if constexpr (kEx) if (mode == kInverseCdf) {
-    __shared__ double s_d[2][kWarps];  // per-warp sums
-    __shared__ long long s_pick;       // chosen chunk, then chosen token
-    __shared__ double s_base;          // weight before the chosen chunk
-    __shared__ double s_loc[2][kThreads];
     // 3'. Inverse CDF with one uniform u: the token is the smallest v whose
     //     cumulative weight exceeds u * S, in vocabulary order; weights
     //     max(0, p_n - q_n) (p_n should those sum to 0), or p_K for the bonus
-    //     token.  Sums in fp64: this CTA's chunk first; the last CTA to arrive
-    //     scans the chunk sums in chunk order, then searches the chunk holding
-    //     the crossing.  Prefix sums are sequential over per-thread partials,
-    //     so consecutive threads' ranges meet exactly and one entry crosses.
+    //     token.  Weights (at most 1, summing to at most about 1) are summed
+    //     exactly as integers in units of 2^-46 (round to nearest): every order
+    //     of summation gives the same sums, which the integer units compute at
+    //     full rate.  This CTA's
+    //     chunk is summed first; the last CTA to arrive scans the chunk sums in
+    //     chunk order, then searches the chunk holding the crossing.
+    __shared__ long long s_d[2][kWarps];  // per-warp sums
+    __shared__ long long s_pick;          // chosen chunk, then chosen token
+    __shared__ long long s_base;          // weight before the chosen chunk
+    __shared__ long long s_loc[2][kThreads];
+    constexpr float kFx = 70368744177664.0f;  // 2^46
+    auto fx = [](float w) { return __float2ll_rn(w * kFx); };
     auto w_p = [&](int64_t v) { return exp2f((pr[v] * inv_t - mp) * kLog2e) * izp; };
     auto w_r = [&](int64_t v) {
       const float rv = w_p(v) - exp2f((qr[v] * inv_t - mq) * kLog2e) * izq;
       return rv > 0.f ? rv : 0.f;
     };
-    double sr = 0.0, sp = 0.0;
+    long long sr = 0, sp = 0;
     for (int64_t v = v0 + tid; v < v1; v += kThreads) {
-      sp += double(w_p(v));
-      if (residual) sr += double(w_r(v));
+      sp += fx(w_p(v));
+      if (residual) sr += fx(w_r(v));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -378,14 +382,14 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       s_d[1][tid >> 5] = sp;
     }
     __syncthreads();
-    double2* csum = reinterpret_cast<double2*>(rpart) + b * race_splits;
+    longlong2* csum = reinterpret_cast<longlong2*>(rpart) + b * race_splits;
     if (tid == 0) {
-      double a = 0.0, c = 0.0;
+      long long a = 0, c = 0;
       for (int w = 0; w < kWarps; ++w) {
         a += s_d[0][w];
         c += s_d[1][w];
       }
-      csum[split] = make_double2(a, c);
+      csum[split] = make_longlong2(a, c);
       __threadfence();
       s_last = atomicAdd(&counter[b], 1) == race_splits - 1;
     }
@@ -395,9 +399,9 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
     // (a) the chunk holding the crossing
     const int per = (race_splits + kThreads - 1) / kThreads;
     const int c_lo = min(race_splits, tid * per), c_hi = min(race_splits, c_lo + per);
-    double lr = 0.0, lpp = 0.0;
+    long long lr = 0, lpp = 0;
     for (int c = c_lo; c < c_hi; ++c) {
-      const double2 t = __ldcg(csum + c);
+      const longlong2 t = __ldcg(csum + c);
       lr += t.x;
       lpp += t.y;
     }
@@ -405,9 +409,9 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
     s_loc[1][tid] = lpp;
     __syncthreads();
     if (tid == 0) {
-      double a = 0.0, c = 0.0;
+      long long a = 0, c = 0;
       for (int t = 0; t < kThreads; ++t) {
-        const double x = s_loc[0][t], y = s_loc[1][t];
+        const long long x = s_loc[0][t], y = s_loc[1][t];
         s_loc[0][t] = a;
         s_loc[1][t] = c;
         a += x;
@@ -418,15 +422,18 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
       s_pick = -1;
     }
     __syncthreads();
-    const bool use_r = residual && s_d[0][0] > 0.0;
-    const double S = use_r ? s_d[0][0] : s_d[1][0];
-    const double target = double(u_res[b]) * S;
+    const bool use_r = residual && s_d[0][0] > 0;
+    const long long S = use_r ? s_d[0][0] : s_d[1][0];
+    // cumulative weight C crosses u * S where C > floor(u * S) (u < 1, so at
+    // most S - 1 even where the product rounds up)
+    const long long target =
+        S > 0 ? min(S - 1, (long long)floor(double(u_res[b]) * double(S))) : 0;
     {
-      const double E = s_loc[use_r ? 0 : 1][tid];
-      double loc = 0.0;
+      const long long E = s_loc[use_r ? 0 : 1][tid];
+      long long loc = 0;
       for (int c = c_lo; c < c_hi; ++c) {
-        const double2 t = __ldcg(csum + c);
-        const double before = E + loc;
+        const longlong2 t = __ldcg(csum + c);
+        const long long before = E + loc;
         loc += use_r ? t.x : t.y;
         if (before <= target && target < E + loc) {
           s_pick = c;
@@ -439,42 +446,40 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
     if (s_pick >= 0) {
       // (b) the entry of that chunk where the cumulative weight crosses u * S
       const int64_t cv0 = s_pick * race_chunk, cv1 = min(V, cv0 + race_chunk);
-      const double base = s_base;
+      const long long base = s_base;
       const int64_t per2 = (cv1 - cv0 + kThreads - 1) / kThreads;
       const int64_t e_lo = min(cv1, cv0 + tid * per2), e_hi = min(cv1, e_lo + per2);
-      double l = 0.0;
-      for (int64_t v = e_lo; v < e_hi; ++v) l += double(use_r ? w_r(v) : w_p(v));
+      long long l = 0;
+      for (int64_t v = e_lo; v < e_hi; ++v) l += fx(use_r ? w_r(v) : w_p(v));
       __syncthreads();
       s_loc[0][tid] = l;
       __syncthreads();
       if (tid == 0) {
-        double a = 0.0;
+        long long a = 0;
         for (int t = 0; t < kThreads; ++t) {
-          const double x = s_loc[0][t];
+          const long long x = s_loc[0][t];
           s_loc[0][t] = a;
           a += x;
         }
         s_pick = -1;
       }
       __syncthreads();
-      const double E = s_loc[0][tid];
-      double loc = 0.0;
+      long long cum = base + s_loc[0][tid];
       int64_t last_pos = -1;
       for (int64_t v = e_lo; v < e_hi; ++v) {
-        const double wv = double(use_r ? w_r(v) : w_p(v));
-        const double before = base + (E + loc);
-        loc += wv;
-        if (wv > 0.0) last_pos = v;
-        if (before <= target && target < base + (E + loc)) s_pick = v;
+        const long long wv = fx(use_r ? w_r(v) : w_p(v));
+        if (wv > 0) last_pos = v;
+        if (cum <= target && target < cum + wv) s_pick = v;
+        cum += wv;
       }
-      s_loc[1][tid] = double(last_pos);
+      s_loc[1][tid] = last_pos;
       __syncthreads();
       tok = s_pick;
       if (tok < 0) {
-        // rounding left the crossing just past this chunk's recomputed sum:
-        // its last entry with positive weight
+        // the sums are exact, so only a chunk whose weights all rounded to 0
+        // can miss: its last entry with positive weight, if any
         for (int t = kThreads - 1; t >= 0 && tok < 0; --t)
-          if (s_loc[1][t] >= 0.0) tok = int64_t(s_loc[1][t]);
+          if (s_loc[1][t] >= 0) tok = s_loc[1][t];
       }
     }
     if (tid == 0) {

@@ -6,7 +6,7 @@ distribution taken at temperature T.)
 
 The race at any T is compared bit-exact outside fp64 near-ties, as the plain
 verifier.  The inverse CDF picks the bucket that holds u * S; the kernel's
-fp32 weights (summed in fp64) move bucket edges by about 2e-7 of S, so its
+fp32 weights (summed exactly in fixed point) move bucket edges by about 2e-7 of S, so its
 token is compared where the oracle's edge margin is at least 1e-6 of S, and
 its distribution is checked by chi-square."""
 import numpy as np
