@@ -179,6 +179,21 @@ def dist_setup(n_gpus):
     return ws, rank, local
 
 
+def aggregate(ms_step, tokens, ws, device):
+    """Whole-job figures over the ranks: the slowest rank's step time and the
+    tokens every rank verified (each rank runs its own replica; this is the
+    only exchange, host-side, outside the timed region)."""
+    if ws == 1:
+        return ms_step, tokens
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 GROUPINGS = {"layer": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
              "all": [["q", "k", "v", "o", "gate", "up", "down"]],
              "single": [["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]]}
@@ -302,15 +317,11 @@ def run_uno(args):
     t_step = [e[0].elapsed_time(e[2]) for e in ev]
     t_proj = [e[0].elapsed_time(e[1]) for e in ev]
     t_ver = [e[1].elapsed_time(e[2]) for e in ev]
-    ms_step = sum(t_step) / K
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
     n_acc, toks, n_em, vstat = (t.cpu() for t in st.vout)
     assert int(vstat.abs().sum()) == 0
-    tokens = int(n_em.sum())
-    value = tokens * ws / (ms_step / 1e3)
+    ms_step, tokens_all = aggregate(sum(t_step) / K, int(n_em.sum()), ws, dev)
+    tokens = tokens_all // ws  # per replica (every replica runs the same seeded step)
+    value = tokens_all / (ms_step / 1e3)
 
     # roofline of the dominant op: the layer's gated-LoRA projections
     by, fl = proj_bytes_flops(st.M, st.n_gate1)
@@ -356,7 +367,7 @@ def run_uno(args):
         out["roofline"]["frac_of_sustained"] = round(achieved / tflops_sustained, 4)
     out["clocks"] = clk.summary()
     if not args.no_e2e:
-        out["e2e"] = e2e(st, dev, max(5, min(K, 50)))
+        out["e2e"] = e2e(st, dev, max(5, min(K, 50)), ws)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         if st.plain:
             out["cpu_baseline"] = cpu_baseline(st, args.batch, args.sigma, budget_s=15.0)
@@ -368,7 +379,7 @@ def run_uno(args):
         torch.distributed.destroy_process_group()
 
 
-def e2e(st, dev, steps):
+def e2e(st, dev, steps, ws=1):
     """Same metric through the public API with host buffers: every step copies
     its inputs host->device from pinned memory, runs the ops eagerly and reads
     the verified tokens back."""
@@ -400,14 +411,15 @@ def e2e(st, dev, steps):
     for _ in range(3):
         one()
     torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
         one()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    tokens = int(outs[1].sum())
+    ms, tokens = aggregate(e0.elapsed_time(e1) / steps, int(outs[1].sum()), ws, dev)
     return {"value": round(tokens / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "launch": "eager API calls"}
