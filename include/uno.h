@@ -148,6 +148,15 @@ typedef struct {
     float alpha;
 } uno_lora_problem;
 
+/* Diagnostic, host only (no GPU, no CUDA call): builds the schedule that
+ * uno_gated_lora_linear_batched would use on a GPU with `sms` SMs and checks
+ * its invariants -- the grid fits one CTA per SM, every section's K-blocks
+ * are partitioned over the CTAs in order, a split T tile's finisher takes no
+ * other work, the workspace regions fit.  Returns 0 when all hold, a positive
+ * invariant number otherwise, or UNO_ERR_ARG / UNO_ERR_UNSUPPORTED for
+ * arguments the projection itself would refuse (pointers are not read). */
+int uno_lora_plan_check(int n, const uno_lora_problem *problems, int64_t M, int dtype, int sms);
+
 size_t uno_gated_lora_linear_batched_workspace(int n, const uno_lora_problem *problems,
                                                int64_t M, int dtype);
 

@@ -60,6 +60,16 @@ class LoraProblemC(ctypes.Structure):
 
 SIGNATURES["uno_gated_lora_linear_batched_workspace"] = (_SZ, [_I, _P, _I64, _I])
 SIGNATURES["uno_gated_lora_linear_batched"] = (_I, [_I, _P, _I64, _I, _P, _SZ, _P])
+SIGNATURES["uno_lora_plan_check"] = (_I, [_I, _P, _I64, _I, _I])
+
+
+def uno_lora_plan_check(shapes, M: int, sms: int, dtype: int = 1) -> int:
+    """Host-only check of the projection schedule for problems given as
+    (d_in, d_out, rank) on a GPU with `sms` SMs: 0 when its invariants hold."""
+    arr = (LoraProblemC * len(shapes))()
+    for i, (di, do, r) in enumerate(shapes):
+        arr[i] = LoraProblemC(0, 0, 0, 0, 0, 0, di, do, r, 1.0)
+    return int(lib().uno_lora_plan_check(len(shapes), ctypes.cast(arr, _P), M, dtype, sms))
 
 _lib = None
 

@@ -107,6 +107,15 @@ size_t uno_gated_lora_linear_batched_workspace(int n, const uno_lora_problem* pr
   return lora_group_workspace_bytes(n, problems, M, dtype, sm_count());
 }
 
+int uno_lora_plan_check(int n, const uno_lora_problem* problems, int64_t M, int dtype, int sms) {
+  if (dtype != UNO_F32 && dtype != UNO_BF16) return UNO_ERR_UNSUPPORTED;
+  if (n < 1 || n > UNO_MAX_LORA_PROBLEMS || !problems || sms < 1 || M < 1) return UNO_ERR_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!lora_shape_ok(M, problems[i].d_in, problems[i].d_out, problems[i].rank, dtype))
+      return UNO_ERR_ARG;
+  return lora_plan_check(n, problems, M, dtype, sms);
+}
+
 int uno_gated_lora_linear_batched(int n, const uno_lora_problem* problems, int64_t M, int dtype,
                                   void* workspace, size_t ws_bytes, uno_stream_t stream) {
   if (dtype != UNO_F32 && dtype != UNO_BF16) return UNO_ERR_UNSUPPORTED;

@@ -55,6 +55,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <memory>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -1323,6 +1324,69 @@ size_t lora_group_workspace_bytes(int n, const uno_lora_problem* pr, int64_t M, 
   Layout L;
   if (!make_layout(n, pr, M, dtype, sms, L)) return 0;
   return L.bytes;
+}
+
+// Host-side invariants of the schedule make_layout builds for `sms` CTAs
+// (no GPU involved): 0 when all hold, else the number of the first that fails.
+int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms) {
+  auto Lp = std::make_unique<Layout>();
+  Layout& L = *Lp;
+  if (!make_layout(n, pr, M, dtype, sms, L)) return 1;
+  const Params& P = L.P;
+  const int G = P.grid;
+  // 2: one CTA per SM, at most the grid the kernel is built for
+  if (G < 1 || G > std::min(sms, kMaxGrid)) return 2;
+  // 3: the phase table: data-parallel phases, then the two stream-K sections
+  if (P.dp0 < 0 || P.dp1 < P.dp0 || P.ph0[0] != P.dp1 || P.ph1[0] < P.ph0[0] ||
+      P.ph0[1] != P.ph1[0] || P.ph1[1] < P.ph0[1] || P.ph1[1] > kMaxPhases)
+    return 3;
+  // 4: data-parallel waves only in tokens-as-M order, and then over every tile
+  if (P.dp_tiles > 0) {
+    int64_t t = 0;
+    for (int p = P.dp0; p < P.dp1; ++p) t += P.ph[p].tiles;
+    if (P.swap || t != P.dp_tiles || P.dp_tiles < G) return 4;
+  }
+  int64_t sec_total[2] = {0, 0};
+  for (int sec = 0; sec < 2; ++sec) {
+    // 5: a section's phases are contiguous runs of whole tiles
+    for (int p = P.ph0[sec]; p < P.ph1[sec]; ++p) {
+      const Phase& f = P.ph[p];
+      if (f.kb_start != sec_total[sec] || f.tiles < 1 || f.nkb < 1 || (f.down != 0) != (sec == kDown))
+        return 5;
+      sec_total[sec] += int64_t(f.tiles) * f.nkb;
+    }
+    // 6: CTA ranges partition the section's K-blocks in CTA order
+    if (P.lo[sec][0] != 0 || P.lo[sec][G] != sec_total[sec]) return 6;
+    for (int c = 0; c < G; ++c)
+      if (P.lo[sec][c + 1] < P.lo[sec][c]) return 6;
+  }
+  // 7: a per-piece adapter needs no T tiles
+  if (P.localt && sec_total[kDown] > 0) return 7;
+  // 8: a CTA that finishes a split T tile has no main work (unless all do)
+  int n_fin = 0, n_fin_busy = 0;
+  for (int c = 0; c < G; ++c) {
+    const int64_t lo0 = P.lo[kDown][c], hi0 = P.lo[kDown][c + 1];
+    if (lo0 >= hi0) continue;
+    for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
+      const Phase& f = P.ph[p];
+      const int64_t end = f.kb_start + int64_t(f.tiles) * f.nkb;
+      if (hi0 - 1 < f.kb_start || hi0 - 1 >= end) continue;
+      const int64_t ts = f.kb_start + (hi0 - 1 - f.kb_start) / f.nkb * f.nkb;
+      if (ts >= lo0 && ts + f.nkb > hi0) {
+        ++n_fin;
+        n_fin_busy += P.lo[kMain][c] < P.lo[kMain][c + 1];
+      }
+    }
+  }
+  if (n_fin_busy > 0 && n_fin < G) return 8;
+  // 9: decode order only for decode-sized M
+  if (P.swap != (M <= kSwapMaxRows ? 1 : 0)) return 9;
+  // 10: workspace regions in order and inside the total
+  if (L.off_partial > L.off_sync || L.off_sync + L.sync_bytes > L.bytes) return 10;
+  // 11: the partial slots hold a tile of the widest phase
+  for (int p = 0; p < P.ph1[1]; ++p)
+    if (P.ph[p].bn > P.bnmax) return 11;
+  return 0;
 }
 
 int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, void* ws,

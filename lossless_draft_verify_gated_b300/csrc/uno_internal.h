@@ -45,5 +45,6 @@ constexpr int kMaxLoraProblems = UNO_MAX_LORA_PROBLEMS;
 size_t lora_group_workspace_bytes(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms);
 int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, void* ws,
                       size_t ws_bytes, cudaStream_t st);
+int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms);
 
 }  // namespace uno
