@@ -72,6 +72,22 @@ def peaks():
         return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def kernel_source_hash():
+    """sha256 (16 hex digits) of the projection kernel's sources with comments
+    and whitespace removed: edits to the code invalidate recorded counters,
+    edits to comments do not."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "ptx.cuh", "uno_internal.h"):
+        with open(os.path.join(ROOT, "lossless_draft_verify_gated_b300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(batch, launches):
     """DRAM bytes per projection launch from the committed ncu summary, or None
     when there is none for this workload or the kernel sources changed since."""
@@ -84,11 +100,7 @@ def profiled_traffic(batch, launches):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        h = hashlib.sha256()
-        for name in ("gemm.cu", "ptx.cuh", "uno_internal.h"):
-            with open(os.path.join(ROOT, "lossless_draft_verify_gated_b300", "csrc", name), "rb") as f:
-                h.update(f.read())
-        if h.hexdigest()[:16] != kv.get("source_sha256_16") or int(kv["launches_per_step"]) != launches:
+        if kernel_source_hash() != kv.get("source_sha256_16") or int(kv["launches_per_step"]) != launches:
             return None
         return int(kv["traffic_bytes_per_launch"])
     except Exception:

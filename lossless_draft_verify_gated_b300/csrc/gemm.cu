@@ -40,7 +40,10 @@
 // accumulator (tcgen05.ld) and store y, T or partials, overlapping the next
 // piece's MMAs.
 // Decode-sized M (<= 128 token rows) swaps the operands so that the weights
-// fill the 128-row MMA side and the tokens are N.
+// fill the 128-row MMA side and the tokens are N; short decode launches give
+// each piece its own share of the adapter instead of shared T tiles.  Larger
+// M takes tiles of 128 tokens x 256 (or 128) outputs and, with at least one
+// tile per CTA, deals whole tiles out in data-parallel waves (no splits).
 // Launches are chained with programmatic dependent launch: each CTA lets the
 // next launch in the stream start at once, and waits (griddepcontrol.wait)
 // for the previous one before it touches global memory, except for L2

@@ -21,6 +21,10 @@
 //             of the residual row (or the bonus row); the last CTA to arrive
 //             (atomic counter, no waiting) merges the chunk winners and writes
 //             the outputs.
+// Sampling variants (uno_verify_block_ex) are separate instantiations of both
+// kernels: logits scaled by 1/T, and optionally the single-uniform inverse CDF
+// in place of the race (exact fixed-point chunk sums; the last CTA finds the
+// crossing).  The temperature-1 race keeps the plain instantiations.
 // Nothing spins, nothing traps: bad data sets a per-sequence status.
 #include <algorithm>
 #include <cfloat>
