@@ -10,6 +10,7 @@ Functions (each documented in uno_oracle.c with the passage it follows):
   gated_lora_linear(x, W, A, B, gate, alpha)  -> y (float64)
   verify_block(p_logits, q_logits, draft, u_accept, u_resample)  -> VerifyResult
   verify_block_ex(..., temperature, mode)  -> VerifyResult (temperature, inverse-CDF resample)
+  lm_head_verify(h_p, h_q, W_p, W_q, draft, u_accept, u_resample)  -> VerifyResult (logits = h.W^T)
   draft_sample(logits, u)  -> (tokens, status, margin)
 """
 from __future__ import annotations
@@ -57,6 +58,9 @@ def _load():
     lib.oracle_verify_block_ex_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
                                                ctypes.c_double, ctypes.c_int, P, P, P, P, P, P]
     lib.oracle_verify_block_ex_f64.restype = ctypes.c_int
+    lib.oracle_lm_head_verify_f64.argtypes = [P, P, P, P, I64, P, P, P, I64, I64, I64, I64,
+                                              P, P, P, P, P, P]
+    lib.oracle_lm_head_verify_f64.restype = ctypes.c_int
     lib.oracle_draft_sample_f64.argtypes = [P, P, I64, I64, P, P, P]
     lib.oracle_draft_sample_f64.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -171,6 +175,33 @@ def verify_block_ex(p_logits, q_logits, draft, u_accept, u_resample, temperature
                                         _ptr(toks), _ptr(n_em), _ptr(st), _ptr(am), _ptr(rm))
     if rc != 0:
         raise RuntimeError(f"oracle_verify_block_ex_f64 failed: {rc}")
+    return VerifyResult(n_acc, toks, n_em, st, am, rm)
+
+
+def lm_head_verify(h_p, h_q, W_p, W_q, draft, u_accept, u_resample) -> VerifyResult:
+    """The verifier on logits h.W^T (AR rows h_p [Bn,Kp,d] with head W_p [V,d],
+    draft rows h_q [Bn,K,d] with head W_q [V,d]), everything in fp64."""
+    lib = _load()
+    hp, hq = _np(h_p, np.float64), _np(h_q, np.float64)
+    Wp, Wq = _np(W_p, np.float64), _np(W_q, np.float64)
+    Bn, Kp, d = hp.shape
+    K = hq.shape[1]
+    V = Wp.shape[0]
+    assert Wp.shape == (V, d) and Wq.shape == (V, d) and hq.shape[2] == d
+    dr = _np(draft, np.int32).reshape(Bn, K)
+    ua = _np(u_accept, np.float32).reshape(Bn, K)
+    ur = _np(u_resample, np.float32).reshape(Bn, V)
+    n_acc = np.zeros(Bn, np.int32)
+    toks = np.full((Bn, K + 1), -1, np.int32)
+    n_em = np.zeros(Bn, np.int32)
+    st = np.zeros(Bn, np.int32)
+    am = np.full((Bn, K), np.inf)
+    rm = np.full(Bn, np.inf)
+    rc = lib.oracle_lm_head_verify_f64(_ptr(hp), _ptr(hq), _ptr(Wp), _ptr(Wq), d, _ptr(dr), _ptr(ua),
+                                       _ptr(ur), Bn, K, Kp, V, _ptr(n_acc), _ptr(toks), _ptr(n_em),
+                                       _ptr(st), _ptr(am), _ptr(rm))
+    if rc != 0:
+        raise RuntimeError(f"oracle_lm_head_verify_f64 failed: {rc}")
     return VerifyResult(n_acc, toks, n_em, st, am, rm)
 
 

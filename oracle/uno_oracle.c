@@ -429,6 +429,139 @@ int oracle_verify_block_ex_f64(const float *p_logits, const float *q_logits,
 }
 
 /* ------------------------------------------------------------------------ */
+/* LM head feeding the verifier.  [Explainer] "The Psi-Spec Sampler": the   */
+/* AR model verifies the drafted block in a single forward pass; its last   */
+/* step is the LM head, logits = h . W^T over the vocabulary, for the AR    */
+/* rows (h_p [Bn,Kp,d], head W_p [V,d]) and the draft rows (h_q [Bn,K,d],   */
+/* head W_q [V,d]; the same matrix when both pathways share the head).      */
+/* The result is the verifier's on those logits, computed here in fp64     */
+/* from the fp64 dot products (no rounding of the logits).                  */
+/* ------------------------------------------------------------------------ */
+static int softmax_dlogits_f64(const double *l, int64_t V, double *prob)
+{
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        if (isnan(l[v]) || (isinf(l[v]) && l[v] > 0)) return 1;
+        if (l[v] > m) m = l[v];
+    }
+    if (isinf(m)) return 1;
+    double z = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        prob[v] = exp(l[v] - m);
+        z += prob[v];
+    }
+    for (int64_t v = 0; v < V; ++v) prob[v] /= z;
+    return 0;
+}
+
+/* logits[v] = sum_k h[k] * W[v, k] */
+static void lm_head_row_f64(const double *h, const double *W, int64_t d, int64_t V, double *logits)
+{
+    for (int64_t v = 0; v < V; ++v) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; ++k) acc += h[k] * W[v * d + k];
+        logits[v] = acc;
+    }
+}
+
+int oracle_lm_head_verify_f64(const double *h_p, const double *h_q, const double *W_p,
+                              const double *W_q, int64_t d, const int32_t *draft,
+                              const float *u_acc, const float *u_res, int64_t Bn, int64_t K,
+                              int64_t Kp, int64_t V, int32_t *n_accepted, int32_t *out_tokens,
+                              int32_t *n_emitted, int32_t *status, double *accept_margin,
+                              double *race_margin)
+{
+    if (Bn < 0 || K < 0 || V <= 0 || d <= 0 || (Kp != K && Kp != K + 1)) return OR_ERR_ARG;
+    if (Bn == 0) return OR_OK;
+    if (!h_p || !W_p || (K > 0 && (!h_q || !W_q || !draft || !u_acc)) || !u_res ||
+        !n_accepted || !out_tokens || !n_emitted || !status)
+        return OR_ERR_ARG;
+    int err = OR_OK;
+
+#pragma omp parallel
+    {
+        double *P = (double *)malloc(sizeof(double) * (size_t)(Kp > 0 ? Kp : 1) * (size_t)V);
+        double *Q = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)V);
+        double *l = (double *)malloc(sizeof(double) * (size_t)V);
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!P || !Q || !l || !r) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t b = 0; b < Bn; ++b) {
+            if (!P || !Q || !l || !r) continue;
+            int32_t *out = out_tokens + b * (K + 1);
+            for (int64_t i = 0; i <= K; ++i) out[i] = -1;
+            if (accept_margin)
+                for (int64_t i = 0; i < K; ++i) accept_margin[b * K + i] = INFINITY;
+            if (race_margin) race_margin[b] = INFINITY;
+            n_accepted[b] = 0;
+            n_emitted[b] = 0;
+            status[b] = OR_SEQ_OK;
+            for (int64_t i = 0; i < K; ++i) {
+                const int32_t x = draft[b * K + i];
+                if (x < 0 || x >= V) status[b] = OR_SEQ_BAD_DRAFT;
+            }
+            /* Step 1: the LM head, then the softmax of every row. */
+            int bad = 0;
+            for (int64_t i = 0; i < Kp; ++i) {
+                lm_head_row_f64(h_p + (b * Kp + i) * d, W_p, d, V, l);
+                bad |= softmax_dlogits_f64(l, V, P + i * V);
+            }
+            for (int64_t i = 0; i < K; ++i) {
+                lm_head_row_f64(h_q + (b * K + i) * d, W_q, d, V, l);
+                bad |= softmax_dlogits_f64(l, V, Q + i * V);
+            }
+            if (bad && status[b] == OR_SEQ_OK) status[b] = OR_SEQ_NONFINITE;
+            if (status[b] != OR_SEQ_OK) continue;
+            /* Step 2: accept x_i iff u_i < min(1, p_i(x_i)/q_i(x_i)). */
+            int64_t n = 0;
+            for (int64_t i = 0; i < K; ++i) {
+                const int32_t x = draft[b * K + i];
+                const double pi = P[i * V + x];
+                const double qi = Q[i * V + x];
+                const double rho = qi > 0.0 ? pi / qi : INFINITY;
+                const double thr = rho < 1.0 ? rho : 1.0;
+                const double u = (double)u_acc[b * K + i];
+                if (accept_margin) accept_margin[b * K + i] = fabs(thr - u);
+                if (u < thr) {
+                    out[i] = x;
+                    ++n;
+                } else {
+                    break;
+                }
+            }
+            n_accepted[b] = (int32_t)n;
+            n_emitted[b] = (int32_t)n;
+            /* Step 3: the residual or bonus token by the exponential race. */
+            const float *ub = u_res + b * V;
+            double *rm = race_margin ? race_margin + b : NULL;
+            if (n < K) {
+                double S = 0.0;
+                for (int64_t v = 0; v < V; ++v) {
+                    const double dd = P[n * V + v] - Q[n * V + v];
+                    r[v] = dd > 0.0 ? dd : 0.0;
+                    S += r[v];
+                }
+                if (S == 0.0)
+                    for (int64_t v = 0; v < V; ++v) r[v] = P[n * V + v];
+                out[n] = race_f64(r, ub, V, rm);
+                n_emitted[b] = (int32_t)(n + 1);
+            } else if (Kp == K + 1) {
+                out[K] = race_f64(P + K * V, ub, V, rm);
+                n_emitted[b] = (int32_t)(K + 1);
+            }
+        }
+        free(P);
+        free(Q);
+        free(l);
+        free(r);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Draft sampling (Psi-Spec linear sampler, drafting half).                 */
 /* [Explainer] "The Psi-Spec Sampler": the linear sampler draws one         */
 /* candidate per token position.  tokens[r] = argmax_v q_r(v) / (-ln u[r,v])*/
