@@ -108,6 +108,29 @@ def test_verify_argument_errors(L):
     assert L.uno_draft_sample(None, None, 0, 10, None, None, None) == 0
 
 
+def test_verify_ex_argument_errors(L):
+    """uno_verify_block_ex: the temperature and the resample mode are checked on
+    the host before anything else, then the same checks as uno_verify_block."""
+    P = ctypes.c_void_p
+    ptrs = [P(256)] * 5
+    outs = [P(256)] * 4
+
+    def call(T=1.0, mode=0, Bn=2, K=4, Kp=4, V=100, ws=P(256), ws_bytes=1 << 20, p0=None):
+        pp = list(ptrs)
+        if p0 is not None:
+            pp[0] = p0
+        return L.uno_verify_block_ex(*pp, Bn, K, Kp, V, T, mode, *outs, ws, ws_bytes, None)
+
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert call(T=T) == -1
+    assert call(mode=2) == -1 and call(mode=-1) == -1
+    assert call(T=0.5, Kp=6) == -1
+    assert call(T=0.5, mode=1, p0=P(258)) == -2
+    assert call(T=2.0, mode=1, ws=P(264)) == -4
+    assert call(T=2.0, mode=1, ws_bytes=8) == -4
+    assert call(T=0.7, mode=1, Bn=0) == 0
+
+
 def test_batched_argument_errors(L):
     from lossless_draft_verify_gated_b300 import binding
     P = binding.LoraProblemC
