@@ -11,6 +11,7 @@ Functions (each documented in uno_oracle.c with the passage it follows):
   verify_block(p_logits, q_logits, draft, u_accept, u_resample)  -> VerifyResult
   verify_block_ex(..., temperature, mode)  -> VerifyResult (temperature, inverse-CDF resample)
   lm_head_verify(h_p, h_q, W_p, W_q, draft, u_accept, u_resample)  -> VerifyResult (logits = h.W^T)
+  tree_verify(logits, parent, token, u_accept, u_resample)  -> TreeResult (tree sampler)
   draft_sample(logits, u)  -> (tokens, status, margin)
 """
 from __future__ import annotations
@@ -61,6 +62,8 @@ def _load():
     lib.oracle_lm_head_verify_f64.argtypes = [P, P, P, P, I64, P, P, P, I64, I64, I64, I64,
                                               P, P, P, P, P, P]
     lib.oracle_lm_head_verify_f64.restype = ctypes.c_int
+    lib.oracle_tree_verify_f64.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, P, P, P, P, P]
+    lib.oracle_tree_verify_f64.restype = ctypes.c_int
     lib.oracle_draft_sample_f64.argtypes = [P, P, I64, I64, P, P, P]
     lib.oracle_draft_sample_f64.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -203,6 +206,43 @@ def lm_head_verify(h_p, h_q, W_p, W_q, draft, u_accept, u_resample) -> VerifyRes
     if rc != 0:
         raise RuntimeError(f"oracle_lm_head_verify_f64 failed: {rc}")
     return VerifyResult(n_acc, toks, n_em, st, am, rm)
+
+
+@dataclass
+class TreeResult:
+    n_accepted: np.ndarray     # [Bn] int32, accepted depth
+    path: np.ndarray           # [Bn, N] int32 accepted node ids, -1 padded
+    out_tokens: np.ndarray     # [Bn, N+1] int32, -1 padded
+    n_emitted: np.ndarray      # [Bn] int32
+    status: np.ndarray         # [Bn] int32
+    accept_margin: np.ndarray  # [Bn, N+1] float64, +inf for nodes not tested
+    race_margin: np.ndarray    # [Bn] float64
+
+
+def tree_verify(logits, parent, token, u_accept, u_resample) -> TreeResult:
+    """Tree sampler's verification: logits [Bn, N+1, V] per node (node 0 the
+    prefix), parent/token [Bn, N+1], u_accept [Bn, N+1], u_resample [Bn, V]."""
+    lib = _load()
+    lg = _np(logits, np.float32)
+    Bn, N1, V = lg.shape
+    N = N1 - 1
+    par = _np(parent, np.int32).reshape(Bn, N1)
+    tok = _np(token, np.int32).reshape(Bn, N1)
+    ua = _np(u_accept, np.float32).reshape(Bn, N1)
+    ur = _np(u_resample, np.float32).reshape(Bn, V)
+    n_acc = np.zeros(Bn, np.int32)
+    pth = np.full((Bn, N), -1, np.int32)
+    toks = np.full((Bn, N1), -1, np.int32)
+    n_em = np.zeros(Bn, np.int32)
+    st = np.zeros(Bn, np.int32)
+    am = np.full((Bn, N1), np.inf)
+    rm = np.full(Bn, np.inf)
+    rc = lib.oracle_tree_verify_f64(_ptr(lg), _ptr(par), _ptr(tok), _ptr(ua), _ptr(ur), Bn, N, V,
+                                    _ptr(n_acc), _ptr(pth), _ptr(toks), _ptr(n_em), _ptr(st),
+                                    _ptr(am), _ptr(rm))
+    if rc != 0:
+        raise RuntimeError(f"oracle_tree_verify_f64 failed: {rc}")
+    return TreeResult(n_acc, pth, toks, n_em, st, am, rm)
 
 
 def draft_sample(logits, u):

@@ -562,6 +562,119 @@ int oracle_lm_head_verify_f64(const double *h_p, const double *h_q, const double
 }
 
 /* ------------------------------------------------------------------------ */
+/* Tree sampler, verification half.  [Explainer] "The Psi-Spec Sampler":    */
+/* the tree sampler takes several candidates (the top K) at each position   */
+/* and verifies them in a prefix tree, keeping the AR model's distribution. */
+/* Each drafted node is a deterministic candidate, i.e. a point-mass draft  */
+/* q = delta_x, for which the speculative rule reads: accept x with         */
+/* probability r(x)/S (r the current residual, S its mass), else remove x   */
+/* from the residual, max(0, r - delta_x), and try the next candidate.      */
+/* Walking down from the root: at the current node test its children in     */
+/* index order (their rank); on an acceptance emit the child's token and    */
+/* move to it; when every child is rejected (or there are none) draw one    */
+/* token from the residual by the exponential race and stop.                */
+/*                                                                          */
+/* logits [Bn, N+1, V]: AR logits for the token after node j (node 0 is the */
+/* committed prefix); parent [Bn, N+1] with parent[0] = -1 and              */
+/* 0 <= parent[j] < j; token [Bn, N+1] (token[0] unused); u_acc [Bn, N+1]   */
+/* (the test of node j uses u_acc[j]); u_res [Bn, V].  Outputs n_accepted   */
+/* [Bn] (accepted depth), path [Bn, N] accepted node ids (-1 padded),       */
+/* out_tokens [Bn, N+1] (-1 padded), n_emitted [Bn], status [Bn]; optional  */
+/* accept_margin [Bn, N+1] |r(x)/S - u| per tested node, race_margin [Bn].  */
+/* ------------------------------------------------------------------------ */
+int oracle_tree_verify_f64(const float *logits, const int32_t *parent, const int32_t *token,
+                           const float *u_acc, const float *u_res, int64_t Bn, int64_t N,
+                           int64_t V, int32_t *n_accepted, int32_t *path, int32_t *out_tokens,
+                           int32_t *n_emitted, int32_t *status, double *accept_margin,
+                           double *race_margin)
+{
+    if (Bn < 0 || N < 0 || V <= 0) return OR_ERR_ARG;
+    if (Bn == 0) return OR_OK;
+    if (!logits || !parent || !token || !u_acc || !u_res || !n_accepted || !path ||
+        !out_tokens || !n_emitted || !status)
+        return OR_ERR_ARG;
+    int err = OR_OK;
+
+#pragma omp parallel
+    {
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!r) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t b = 0; b < Bn; ++b) {
+            if (!r) continue;
+            const int32_t *par = parent + b * (N + 1);
+            const int32_t *tok = token + b * (N + 1);
+            int32_t *out = out_tokens + b * (N + 1);
+            int32_t *pth = path + b * N;
+            for (int64_t i = 0; i <= N; ++i) out[i] = -1;
+            for (int64_t i = 0; i < N; ++i) pth[i] = -1;
+            if (accept_margin)
+                for (int64_t i = 0; i <= N; ++i) accept_margin[b * (N + 1) + i] = INFINITY;
+            if (race_margin) race_margin[b] = INFINITY;
+            n_accepted[b] = 0;
+            n_emitted[b] = 0;
+            status[b] = OR_SEQ_OK;
+            /* a tree in topological order with tokens inside the vocabulary */
+            int ok = par[0] == -1;
+            for (int64_t j = 1; j <= N; ++j)
+                ok &= par[j] >= 0 && par[j] < j && tok[j] >= 0 && tok[j] < V;
+            if (!ok) {
+                status[b] = OR_SEQ_BAD_DRAFT;
+                continue;
+            }
+            int64_t cur = 0, depth = 0;
+            while (1) {
+                if (softmax_row_f64(logits + (b * (N + 1) + cur) * V, V, r)) {
+                    status[b] = OR_SEQ_NONFINITE;
+                    break;
+                }
+                double S = 1.0;
+                int64_t acc = -1;
+                for (int64_t j = cur + 1; j <= N && acc < 0; ++j) {
+                    if (par[j] != cur) continue;
+                    const int32_t x = tok[j];
+                    const double thr = S > 0.0 ? r[x] / S : 0.0;
+                    const double u = (double)u_acc[b * (N + 1) + j];
+                    if (accept_margin) accept_margin[b * (N + 1) + j] = fabs(thr - u);
+                    if (u < thr) {
+                        acc = j;
+                    } else {
+                        S -= r[x];
+                        r[x] = 0.0;
+                    }
+                }
+                if (acc >= 0) {
+                    out[depth] = tok[acc];
+                    pth[depth] = (int32_t)acc;
+                    ++depth;
+                    cur = acc;
+                    continue;
+                }
+                /* every child rejected: one token from the residual (from
+                 * p itself should rounding have emptied the residual) */
+                double mass = 0.0;
+                for (int64_t v = 0; v < V; ++v) mass += r[v];
+                if (!(mass > 0.0)) softmax_row_f64(logits + (b * (N + 1) + cur) * V, V, r);
+                out[depth] = race_f64(r, u_res + b * V, V, race_margin ? race_margin + b : NULL);
+                break;
+            }
+            if (status[b] != OR_SEQ_OK) {
+                for (int64_t i = 0; i <= N; ++i) out[i] = -1;
+                for (int64_t i = 0; i < N; ++i) pth[i] = -1;
+                continue;
+            }
+            n_accepted[b] = (int32_t)depth;
+            n_emitted[b] = (int32_t)(depth + 1);
+        }
+        free(r);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Draft sampling (Psi-Spec linear sampler, drafting half).                 */
 /* [Explainer] "The Psi-Spec Sampler": the linear sampler draws one         */
 /* candidate per token position.  tokens[r] = argmax_v q_r(v) / (-ln u[r,v])*/
