@@ -34,7 +34,7 @@
  *       sampler draws a single token at each position).  Pinned by chi-square
  *       against softmax(logits).
  *
- * Readings where the pages are silent (each restated in the design doc):
+ * Readings where the pages are silent (the plainest reading in each case):
  *   - LoRA scale alpha/rank; layouts W[d_out,d_in], A[rank,d_in], B[d_out,rank].
  *   - Temperature 1 on the raw logits.
  *   - Accept draft i iff u_i < min(1, p_i(x_i)/q_i(x_i)), u_i in [0,1).

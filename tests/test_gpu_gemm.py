@@ -195,3 +195,26 @@ def test_batched_deterministic():
     b = _batched([pr for _, pr in layer])
     for ya, yb in zip(a, b):
         assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+
+
+LAYER_GROUPS = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]
+
+
+@pytest.mark.parametrize("M", [256, 1024, 4096, 16384])
+def test_layer_groups_sweep_sampled(M):
+    """The layer's projections as the benchmark launches them (one grouped
+    launch each for q/k/v, o, gate/up and down) at the row counts of the batch
+    sweep (batch 8, 32, 128, 512 x 2 x block 16): 64 seeded rows, half gate 0
+    and half gate 1, against the oracle over every column."""
+    layer = dict(inputs.llama3_layer(M, rank=128, alpha=256.0, block=16))
+    g = inputs.generator(f"rows.sweep.{M}")
+    perm = torch.randperm(M, generator=g)
+    gate = layer["q"].gate
+    rows = torch.cat([perm[gate[perm] == 0][:32], perm[gate[perm] == 1][:32]])
+    for names in LAYER_GROUPS:
+        ys = _batched([layer[n] for n in names])
+        for n, y in zip(names, ys):
+            assert gemm_err(y[rows.cuda()], _ref(layer[n], rows)) <= GEMM_TOL, (M, n)
+        del ys
+    from lossless_draft_verify_gated_b300 import uno_device_error
+    assert uno_device_error() == 0
