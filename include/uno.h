@@ -28,7 +28,9 @@
  *     where an argument says otherwise.  The library allocates no device or
  *     host memory on the compute path and keeps no per-call state.  (It
  *     caches the driver entry point used to encode TMA descriptors and the
- *     per-device SM count and kernel attributes.)
+ *     per-device SM count and kernel attributes; these caches assume that
+ *     the process does not call cudaDeviceReset and then use the library
+ *     again.)
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call is asynchronous and stream-ordered; the library never
  *     synchronises.  Workspace must not be shared by calls that may overlap
@@ -103,6 +105,13 @@ enum {
  * give the same bits on every call.
  * Requirements: M >= 0, d_in >= 1, d_out >= 1, rank in [0, 256], d_in,
  * d_out and rank multiples of 8; alpha finite.  rank == 0 gives x.W^T.
+ * Residency: the kernel is persistent (one CTA per SM) and some CTAs wait,
+ * with a 2-second limit, for partial sums that later-started CTAs of the
+ * same launch publish.  When other work keeps SMs from this launch (another
+ * stream's long kernel, an MPS or green-context SM limit) such a wait can run
+ * out; the CTA then skips its output tile and sets bit 0 of the device error
+ * word.  y is therefore defined only when uno_device_error() reads 0 after
+ * the call; a caller that shares the GPU should check it.
  * The workspace query returns the bytes for the device current at the time
  * of the call; use the same device for the compute call.
  * ------------------------------------------------------------------------- */
@@ -262,6 +271,92 @@ int uno_verify_block_no_alloc(const float *p_logits, const float *q_logits,
                               int32_t *status, uno_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * LM head + block verifier: the verifying forward pass ends in the LM head,
+ * logits = h . W^T, whose rows feed the block verifier ("Unlocking Lossless
+ * Speedups in LLMs via Discrete Diffusion", aifromscratch.in, "The Psi-Spec
+ * Sampler"; aiany.app summary, "Key Findings": one forward pass of the AR
+ * model verifies the drafted block).  The result is uno_verify_block's on
+ * p = the AR rows' logits and q = the draft rows' logits, with one LM head
+ * W shared by both pathways (the adapter of the draft pathway sits in the
+ * projections, not in the head).
+ *
+ *   h          [Bn*Kp + Bn*K, d] bf16 final hidden states: the AR rows of
+ *              every sequence (row b*Kp + j), then the draft rows (row
+ *              Bn*Kp + b*K + i)
+ *   W          [V, d] bf16 LM head (nn.Linear layout)
+ *   draft, u_accept, u_resample, outputs: as uno_verify_block
+ *   mode       UNO_LM_PLAIN: the head GEMM stores every logit (fp32) and the
+ *                block verifier reads them;
+ *              UNO_LM_STATS_STORE: the GEMM's epilogue leaves each row's
+ *                softmax statistics and drafted-token logit, the accept
+ *                decisions use those, and only the resampled rows are read
+ *                back from the stored logits;
+ *              UNO_LM_STATS_RECOMPUTE: the epilogue leaves only the
+ *                statistics (no logit reaches memory); the two rows per
+ *                sequence that the resample needs are recomputed;
+ *              UNO_LM_AUTO: one of the two statistics modes by batch size.
+ *              All modes compute the same function (bf16 operands, fp32
+ *              accumulation; they may differ in the last bits of a logit).
+ *   workspace  at least uno_lm_head_verify_workspace(Bn, K, Kp, V, d, mode)
+ *              bytes, 256-byte aligned, contents ignored on entry.
+ * Requirements: as uno_verify_block, plus d >= 8 and V multiples of 8, and
+ * h, W, u_resample 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+enum { UNO_LM_AUTO = 0, UNO_LM_PLAIN = 1, UNO_LM_STATS_STORE = 2, UNO_LM_STATS_RECOMPUTE = 3 };
+
+size_t uno_lm_head_verify_workspace(int64_t Bn, int64_t K, int64_t Kp, int64_t V,
+                                    int64_t d, int mode);
+
+int uno_lm_head_verify(const void *h, const void *W, const int32_t *draft,
+                       const float *u_accept, const float *u_resample, int64_t Bn,
+                       int64_t K, int64_t Kp, int64_t V, int64_t d, int mode,
+                       int32_t *n_accepted, int32_t *out_tokens,
+                       int32_t *n_emitted, int32_t *status, void *workspace,
+                       size_t ws_bytes, uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Tree verifier (Psi-Spec tree sampler, verification half): several drafted
+ * candidates per position, arranged in a prefix tree, verified so that the
+ * emitted tokens keep the AR model's distribution ("Unlocking Lossless
+ * Speedups in LLMs via Discrete Diffusion", aifromscratch.in, "The Psi-Spec
+ * Sampler": the tree sampler takes the top K candidates at each position and
+ * verifies them in a prefix tree, best at low batch sizes).
+ *
+ * Node 0 is the committed prefix; nodes 1..N are drafted tokens.  Every node
+ * is a deterministic candidate, for which the lossless rule is, from the root:
+ * with r = p_cur (softmax of logits[b,cur,:]) and S = 1, test the children of
+ * cur in index order: accept child j (token x = token[b,j]) iff
+ * u_accept[b,j] < r(x)/S; else S -= r(x), r(x) = 0 and test the next child.
+ * An acceptance emits x and moves to j; when every child is rejected (or
+ * there is none) one token is drawn from r (from p_cur should r be all zero)
+ * by the exponential race argmax_v r(v) / (-ln u_resample[b,v]), and the walk
+ * stops.  n_accepted = tokens accepted, n_emitted = n_accepted + 1.
+ *
+ *   logits     [Bn, N+1, V] float32: AR logits of the token after node j
+ *   parent     [Bn, N+1]    int32: parent[b,0] = -1, 0 <= parent[b,j] < j
+ *   token      [Bn, N+1]    int32: the token of node j (token[b,0] unused)
+ *   u_accept   [Bn, N+1]    float32 in [0,1): u_accept[b,j] tests node j
+ *   u_resample [Bn, V]      float32 in (0,1)
+ *   n_accepted [Bn], path [Bn, N] (accepted node ids by depth, -1 padded;
+ *   may be NULL when N = 0), out_tokens [Bn, N+1] (-1 padded), n_emitted
+ *   [Bn], status [Bn] int32 outputs.  A malformed tree (parent or token out
+ *   of range) gives UNO_SEQ_BAD_DRAFT; a NaN or +inf logit, or an all -inf
+ *   row, at a node the walk reaches gives UNO_SEQ_NONFINITE; either way the
+ *   sequence emits nothing (outputs -1, counts 0).
+ *   workspace  at least uno_tree_verify_workspace(Bn, N, V) bytes, 256-byte
+ *              aligned, contents ignored on entry.
+ * Requirements: Bn >= 0, 0 <= N <= 255, 1 <= V < 2^31.
+ * ------------------------------------------------------------------------- */
+size_t uno_tree_verify_workspace(int64_t Bn, int64_t N, int64_t V);
+
+int uno_tree_verify(const float *logits, const int32_t *parent,
+                    const int32_t *token, const float *u_accept,
+                    const float *u_resample, int64_t Bn, int64_t N, int64_t V,
+                    int32_t *n_accepted, int32_t *path, int32_t *out_tokens,
+                    int32_t *n_emitted, int32_t *status, void *workspace,
+                    size_t ws_bytes, uno_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Draft sampling (Psi-Spec linear sampler, drafting half: a single token at
  * each position; "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
  * aifromscratch.in, "The Psi-Spec Sampler").
@@ -277,6 +372,8 @@ int uno_draft_sample(const float *logits, const float *u, int64_t R, int64_t V,
 /* Device error word of this library on the current device (synchronous).
  * Bit 0 is set when a pipeline wait inside a projection kernel exceeded its
  * 2-second limit; that kernel unwound without writing its output tile.
+ * Bit 1 is set when a wait of the one-launch verifier (small batches) ran out;
+ * that call's outputs are invalid.
  * reset != 0 clears the word.  Returns the word (>= 0) or UNO_ERR_CUDA. */
 int uno_device_error(int reset);
 

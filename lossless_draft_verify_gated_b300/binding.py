@@ -45,6 +45,11 @@ SIGNATURES = {
     "uno_verify_block_no_alloc_max_scratch": (_SZ, []),
     "uno_verify_block_no_alloc": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
                                        _P]),
+    "uno_lm_head_verify_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
+    "uno_lm_head_verify": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P,
+                                _P, _SZ, _P]),
+    "uno_tree_verify_workspace": (_SZ, [_I64, _I64, _I64]),
+    "uno_tree_verify": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "uno_device_error": (_I, [_I]),
     "uno_status_string": (ctypes.c_char_p, [_I]),
     "uno_version": (_I, []),
@@ -151,7 +156,24 @@ def uno_gated_lora_linear(x, W, A, B, gate, alpha, *, y=None, workspace=None, st
     return y
 
 
+_PROBLEM_ARRAYS = {}
+
+
 def _problems(problems):
+    # repeated calls with the same tensors (a decode loop) reuse the marshalled array
+    key = tuple((t.data_ptr(), tuple(t.shape), t.device.index, t.is_contiguous()) for p in problems
+                for t in (p[0], p[1], p[2], p[3], p[4], p[6])) + tuple(float(p[5]) for p in problems)
+    arr = _PROBLEM_ARRAYS.get(key)
+    if arr is not None:
+        return arr
+    arr = _marshal_problems(problems)
+    if len(_PROBLEM_ARRAYS) > 64:
+        _PROBLEM_ARRAYS.clear()
+    _PROBLEM_ARRAYS[key] = arr
+    return arr
+
+
+def _marshal_problems(problems):
     arr = (LoraProblemC * len(problems))()
     for i, (x, W, A, B, gate, alpha, y) in enumerate(problems):
         for t in (x, W, gate, y) + ((A, B) if A.numel() else ()):
@@ -240,6 +262,73 @@ def uno_verify_block_ex(p_logits, q_logits, draft, u_accept, u_resample, *, temp
                                    _dptr(st), _dptr(workspace), workspace.numel(), _stream(stream))
     _check("uno_verify_block_ex", rc)
     return n_acc, toks, n_em, st
+
+
+UNO_LM_AUTO = 0
+UNO_LM_PLAIN = 1
+UNO_LM_STATS_STORE = 2
+UNO_LM_STATS_RECOMPUTE = 3
+_LM_MODE = {"auto": UNO_LM_AUTO, "plain": UNO_LM_PLAIN, "stats_store": UNO_LM_STATS_STORE,
+            "stats_recompute": UNO_LM_STATS_RECOMPUTE}
+
+
+def uno_lm_head_verify_workspace(Bn, K, Kp, V, d, mode="auto") -> int:
+    return int(lib().uno_lm_head_verify_workspace(Bn, K, Kp, V, d, _LM_MODE[mode]))
+
+
+def uno_lm_head_verify(h, W, draft, u_accept, u_resample, *, Kp=None, mode="auto", out=None,
+                       workspace=None, stream=None):
+    """LM head + block verifier.  h [Bn*Kp + Bn*K, d] bf16 (AR rows of every
+    sequence, then draft rows), W [V, d] bf16, draft/u_accept [Bn, K],
+    u_resample [Bn, V].  Returns (n_accepted, out_tokens, n_emitted, status)."""
+    Bn, K = draft.shape
+    Kp = K if Kp is None else Kp
+    V, d = W.shape
+    assert h.shape == (Bn * (Kp + K), d)
+    dev = h.device
+    if out is None:
+        out = (torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty((Bn, K + 1), dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev))
+    n_acc, toks, n_em, st = out
+    if workspace is None:
+        workspace = _workspace(uno_lm_head_verify_workspace(Bn, K, Kp, V, d, mode), dev)
+    rc = lib().uno_lm_head_verify(_dptr(h), _dptr(W), _dptr(draft), _dptr(u_accept),
+                                  _dptr(u_resample), Bn, K, Kp, V, d, _LM_MODE[mode], _dptr(n_acc),
+                                  _dptr(toks), _dptr(n_em), _dptr(st), _dptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    _check("uno_lm_head_verify", rc)
+    return n_acc, toks, n_em, st
+
+
+def uno_tree_verify_workspace(Bn, N, V) -> int:
+    return int(lib().uno_tree_verify_workspace(Bn, N, V))
+
+
+def uno_tree_verify(logits, parent, token, u_accept, u_resample, *, out=None, workspace=None,
+                    stream=None):
+    """Tree sampler's verification.  logits [Bn, N+1, V], parent/token/u_accept
+    [Bn, N+1], u_resample [Bn, V].  Returns (n_accepted [Bn], path [Bn, N],
+    out_tokens [Bn, N+1], n_emitted [Bn], status [Bn]), int32."""
+    Bn, N1, V = logits.shape
+    N = N1 - 1
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty((Bn, N), dtype=torch.int32, device=dev),
+               torch.empty((Bn, N1), dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev),
+               torch.empty(Bn, dtype=torch.int32, device=dev))
+    n_acc, pth, toks, n_em, st = out
+    if workspace is None:
+        workspace = _workspace(uno_tree_verify_workspace(Bn, N, V), dev)
+    rc = lib().uno_tree_verify(_dptr(logits), _dptr(parent), _dptr(token), _dptr(u_accept),
+                               _dptr(u_resample), Bn, N, V, _dptr(n_acc),
+                               _dptr(pth) if N > 0 else None, _dptr(toks), _dptr(n_em), _dptr(st),
+                               _dptr(workspace), workspace.numel(), _stream(stream))
+    _check("uno_tree_verify", rc)
+    return n_acc, pth, toks, n_em, st
 
 
 def uno_draft_sample(logits, u, *, tokens=None, status=None, stream=None):

@@ -42,6 +42,8 @@ bool lora_shape_ok(int64_t M, int64_t d_in, int64_t d_out, int64_t rank, int dty
   return true;
 }
 
+}  // namespace
+
 bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V) {
   if (Bn < 0 || K < 0 || K > 256 || V < 1 || V >= (int64_t(1) << 31)) return false;
   if (Kp != K && Kp != K + 1) return false;
@@ -50,7 +52,6 @@ bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V) {
   return true;
 }
 
-}  // namespace
 }  // namespace uno
 
 using namespace uno;
@@ -193,6 +194,74 @@ int uno_verify_block_ex(const float* p_logits, const float* q_logits, const int3
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
 
+namespace {
+bool lm_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int64_t d, int mode) {
+  if (!verify_shape_ok(Bn, K, Kp, V)) return false;
+  if (d < 8 || d % 8 || V % 8 || d > (int64_t(1) << 31) - 1) return false;
+  if (mode < UNO_LM_AUTO || mode > UNO_LM_STATS_RECOMPUTE) return false;
+  if (Bn * (Kp + K) > (int64_t(1) << 31) - 1) return false;
+  return true;
+}
+}  // namespace
+
+size_t uno_lm_head_verify_workspace(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int64_t d,
+                                    int mode) {
+  if (!lm_shape_ok(Bn, K, Kp, V, d, mode) || Bn == 0) return 0;
+  return plan_lm_head(Bn, K, Kp, V, d, mode, sm_count()).bytes;
+}
+
+int uno_lm_head_verify(const void* h, const void* W, const int32_t* draft, const float* u_accept,
+                       const float* u_resample, int64_t Bn, int64_t K, int64_t Kp, int64_t V,
+                       int64_t d, int mode, int32_t* n_accepted, int32_t* out_tokens,
+                       int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
+                       uno_stream_t stream) {
+  if (!lm_shape_ok(Bn, K, Kp, V, d, mode)) return UNO_ERR_ARG;
+  if (Bn == 0) return UNO_OK;
+  if (!h || !W || !u_resample || !n_accepted || !out_tokens || !n_emitted || !status || !workspace)
+    return UNO_ERR_ARG;
+  if (K > 0 && (!draft || !u_accept)) return UNO_ERR_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(u_resample) ||
+      (reinterpret_cast<uintptr_t>(u_accept) & 3u))
+    return UNO_ERR_ALIGN;
+  if (!aligned256(workspace)) return UNO_ERR_WORKSPACE;
+  const LmPlan L = plan_lm_head(Bn, K, Kp, V, d, mode, sm_count());
+  if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
+  return launch_lm_head_verify(h, W, draft, u_accept, u_resample, Bn, K, Kp, V, d, n_accepted,
+                               out_tokens, n_emitted, status, workspace, ws_bytes, L,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t uno_tree_verify_workspace(int64_t Bn, int64_t N, int64_t V) {
+  if (Bn < 0 || Bn > (int64_t(1) << 24) || N < 0 || N > kTreeMaxNodes || V < 1 ||
+      V >= (int64_t(1) << 31))
+    return 0;
+  return plan_verify(Bn, 0, N + 1, V, sm_count()).bytes;
+}
+
+int uno_tree_verify(const float* logits, const int32_t* parent, const int32_t* token,
+                    const float* u_accept, const float* u_resample, int64_t Bn, int64_t N,
+                    int64_t V, int32_t* n_accepted, int32_t* path, int32_t* out_tokens,
+                    int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
+                    uno_stream_t stream) {
+  if (Bn < 0 || Bn > (int64_t(1) << 24) || N < 0 || N > kTreeMaxNodes || V < 1 ||
+      V >= (int64_t(1) << 31))
+    return UNO_ERR_ARG;
+  if (Bn == 0) return UNO_OK;
+  if (!logits || !parent || !token || !u_accept || !u_resample || !n_accepted ||
+      (N > 0 && !path) || !out_tokens || !n_emitted || !status || !workspace)
+    return UNO_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(u_resample) |
+       reinterpret_cast<uintptr_t>(u_accept)) & 3u)
+    return UNO_ERR_ALIGN;
+  if (!aligned256(workspace)) return UNO_ERR_WORKSPACE;
+  const VerifyPlan pl = plan_verify(Bn, 0, N + 1, V, sm_count());
+  if (ws_bytes < pl.bytes) return UNO_ERR_WORKSPACE;
+  const cudaError_t e = launch_tree_verify(logits, parent, token, u_accept, u_resample, Bn, N, V,
+                                           n_accepted, path, out_tokens, n_emitted, status,
+                                           workspace, pl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
+}
+
 int uno_draft_sample(const float* logits, const float* u, int64_t R, int64_t V, int32_t* tokens,
                      int32_t* status, uno_stream_t stream) {
   if (R < 0 || V < 1 || V >= (int64_t(1) << 31) || R >= (int64_t(1) << 31)) return UNO_ERR_ARG;
@@ -205,6 +274,12 @@ int uno_draft_sample(const float* logits, const float* u, int64_t R, int64_t V, 
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
 
-int uno_device_error(int reset) { return read_device_error(reset); }
+int uno_device_error(int reset) {
+  const int g = read_device_error(reset);
+  if (g < 0) return g;
+  const int v = read_verify_error(reset);
+  if (v < 0) return v;
+  return g | (v << 1);
+}
 
 }  // extern "C"

@@ -63,6 +63,7 @@
 
 #include "ptx.cuh"
 #include "uno_internal.h"
+#include "verify_common.cuh"
 
 namespace uno {
 
@@ -114,6 +115,17 @@ struct Prob {
   int r;
   int tflag0;  // first T-ready flag of the problem
   int ttiles;  // T tiles of the problem
+  int f32out;  // store y as fp32 (bf16 operands)
+  // Statistics epilogue (logit rows of the verifier, rank 0): instead of (or
+  // besides, st_store) storing y, every finished tile leaves per row the
+  // (max, sum exp) of its columns in st_part[row * st_nvt + vocab tile] and
+  // the logit of the row's drafted token in st_gather[row].  Rows are grouped
+  // per sequence as st_Kp AR rows then st_K draft rows.
+  int st_store;
+  int st_K, st_Kp, st_Rp, st_nvt;
+  const int32_t* st_draft;
+  float2* st_part;
+  float* st_gather;
 };
 
 struct Params {
@@ -398,7 +410,7 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
 #pragma unroll
         for (int j = 0; j < 8; ++j) r[j] *= gs;
       }
-      if (!f.down && P.out_f32) {
+      if (!f.down && (P.out_f32 || pb.f32out)) {
         float4* d = reinterpret_cast<float4*>(static_cast<float*>(pb.y) + int64_t(m) * ncols + n);
         d[0] = make_float4(r[0], r[1], r[2], r[3]);
         d[1] = make_float4(r[4], r[5], r[6], r[7]);
@@ -418,7 +430,7 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
     if (m >= P.M) return;
     const int n0 = tb * f.bn + c0;
     const float gs = f.down ? float(pb.gate[m]) * pb.scale : 1.f;
-    if (!f.down && P.out_f32) {
+    if (!f.down && (P.out_f32 || pb.f32out)) {
       float* d = static_cast<float*>(pb.y) + int64_t(m) * ncols;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -449,14 +461,93 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// ---------------------------------------------------------- statistics epilogue
+// Drafted token of logit row m (-1 for a bonus AR row).  Rows: the st_Rp AR
+// rows (sequence b, position j at b*Kp + j), then the draft rows (b, i) at
+// st_Rp + b*K + i.
+__device__ __forceinline__ int row_draft_token(const Prob& pb, int m) {
+  if (m < pb.st_Rp) {
+    const int b = m / pb.st_Kp, j = m - b * pb.st_Kp;
+    return j < pb.st_K ? pb.st_draft[int64_t(b) * pb.st_K + j] : -1;
+  }
+  return pb.st_draft[m - pb.st_Rp];
+}
+
+// Decode order (lane = vocabulary entry n, accumulator column = token): the
+// (max, sum exp) of 16 tokens over this warp's 32 entries by butterflies, then
+// over the tile's 4 warps through shared memory; one partial per (token, tile).
+// All 128 epilogue threads call it together.
+__device__ __forceinline__ void stats16_swap(const Params& P, const Phase& f, const Prob& pb, int ta,
+                                             int tb, int row, int c0, const float (&v)[16],
+                                             const int* xd_s, float2* red, int et) {
+  const int n = ta * kBM + row;
+  const bool okn = n < pb.d_out;
+  const int lane = row & 31, q = row >> 5;
+  float mx[16], sm[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) mx[j] = okn ? v[j] : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sm[j] = (okn && mx[j] != -INFINITY) ? __expf(v[j] - mx[j]) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sm[j] += __shfl_xor_sync(0xffffffffu, sm[j], o);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int m = tb * f.bn + c0 + j;
+    if (okn && m < P.M && xd_s[m] == n) pb.st_gather[m] = v[j];
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) red[q * 16 + j] = make_float2(mx[j], sm[j]);
+  }
+  epi_sync();
+  if (et < 16) {
+    const int m = tb * f.bn + c0 + et;
+    vfy::MS t{-INFINITY, 0.f};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float2 r = red[w * 16 + et];
+      t = vfy::ms_merge(t, vfy::MS{r.x, r.y});
+    }
+    if (m < P.M) pb.st_part[int64_t(m) * pb.st_nvt + ta] = make_float2(t.m, t.s);
+  }
+  epi_sync();
+}
+
+// Large-M order (lane = token row m, accumulator column = vocabulary entry):
+// a running (max, sum exp) per thread over the tile's columns; stats_end
+// writes it once the tile's last columns are in.
+__device__ __forceinline__ void stats16_rows(const Phase& f, const Prob& pb, int tb, int c0,
+                                             const float (&v)[16], int xd, int m_ok, float* gather_m,
+                                             vfy::MS& acc) {
+  const int n0 = tb * f.bn + c0;
+  float x[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = n0 + j < pb.d_out ? v[j] : -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 16; j += 4) vfy::ms_add4(acc, x[j], x[j + 1], x[j + 2], x[j + 3]);
+  if (m_ok && xd >= n0 && xd < n0 + 16) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (xd == n0 + j) *gather_m = v[j];
+  }
+}
+
 // SWAP: decode-sized M, the weights are the A operand (128 rows of W per
 // tile) and the tokens are N.  LOCALT (swap only): every piece computes its
 // own share of T = x.A^T and applies it; otherwise T is computed once per
 // T tile in the down section and read back by TMA.
-template <int BNMAX, bool SWAP, bool LOCALT>
+// STATS: the statistics epilogue of the verifier's logit rows (rank 0 only).
+template <int BNMAX, bool SWAP, bool LOCALT, bool STATS>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params Pk) {
   static_assert(SWAP || !LOCALT, "per-piece adapter needs the swapped operands");
+  static_assert(!(STATS && LOCALT), "the statistics epilogue has no adapter");
   constexpr int STAGES = stages_for<BNMAX, LOCALT>();
   constexpr uint32_t kStage = stage_bytes<BNMAX, LOCALT>();  // A sub-tile, B slot, (LOCALT) down slice
   constexpr uint32_t kBSlot = uint32_t(BNMAX) * kBK * 2;
@@ -738,10 +829,20 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
     const int et = threadIdx.x - 64;
     uint32_t stg_phase = 0;  // phases of stg_bar used so far
     uint32_t tcount = 0;     // (swap) T drains so far
-    if (SWAP) {
+    // (STATS, decode order) the drafted token of every row, and the shared
+    // area of the cross-warp reduction, in place of the gates
+    int* xd_s = reinterpret_cast<int*>(gate_s);
+    float2* st_red = reinterpret_cast<float2*>(gate_s + kSwapMaxRows * 4);
+    if (SWAP && !STATS) {
       // the gates, read where they are needed, are one shared-memory load away
+      // (a problem without an adapter reads none: its gate may be absent)
       for (int p = 0; p < P.nprob; ++p)
-        for (int m = et; m < P.M; m += kEpiThreads) gate_s[p * int(kSwapMaxRows) + m] = P.pb[p].gate[m];
+        for (int m = et; m < P.M; m += kEpiThreads)
+          gate_s[p * int(kSwapMaxRows) + m] = P.pb[p].r > 0 ? P.pb[p].gate[m] : uint8_t(0);
+      epi_sync();
+    }
+    if (SWAP && STATS) {
+      for (int m = et; m < P.M; m += kEpiThreads) xd_s[m] = row_draft_token(P.pb[0], m);
       epi_sync();
     }
     int seg = 0;
@@ -759,6 +860,30 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
         const bool finisher = !whole && g.s == g.tstart;
         const int c1 = finisher ? owner_of(P, sec, g.tend - 1) : cta;
         bool fail = false;
+        // The tile's final values leave through emit (16 columns at a time, in
+        // column order) and emit_end (after its last columns).
+        vfy::MS sacc{-INFINITY, 0.f};
+        const int m_row = ta * kBM + row;  // (large-M order) this thread's token row
+        const int xd_row = (STATS && !SWAP && m_row < P.M) ? row_draft_token(pb, m_row) : -1;
+        float dummy_gather;
+        auto emit = [&](int c0, const float (&v)[16]) {
+          if constexpr (STATS) {
+            if (pb.st_store) store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+            if constexpr (SWAP) {
+              stats16_swap(P, f, pb, ta, tb, row, c0, v, xd_s, st_red, et);
+            } else {
+              stats16_rows(f, pb, tb, c0, v, xd_row, m_row < P.M,
+                           m_row < P.M ? pb.st_gather + m_row : &dummy_gather, sacc);
+            }
+          } else {
+            store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+          }
+        };
+        auto emit_end = [&]() {
+          if constexpr (STATS && !SWAP) {
+            if (m_row < P.M) pb.st_part[int64_t(m_row) * pb.st_nvt + tb] = make_float2(sacc.m, sacc.s);
+          }
+        };
         if (LOCALT && pb.r > 0) {
           // The piece's T (lane = rank, column = token) becomes T' =
           // bf16(gate * scale * T) in shared memory, K-major with the 128-byte
@@ -874,8 +999,9 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             for (int c0 = 0; c0 < f.bn; c0 += 16) {
               float v[16];
               tmem_ld16f(tq + c0, v);
-              store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+              emit(c0, v);
             }
+            emit_end();
           } else if (!finisher) {
             // contributor: leave the piece as a partial and raise this CTA's flag
             float4* dst = reinterpret_cast<float4*>(P.partial + (size_t(cta) * 2 + sec) * kSlot);
@@ -938,11 +1064,12 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                       v[4 * j4 + 3] += t.w;
                     }
                   }
-                  if (b0 + nb >= nc) store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+                  if (b0 + nb >= nc) emit(c0, v);
                 }
                 if (nb > 0) epi_sync();  // the ring is refilled only once every thread has read it
               }
             }
+            emit_end();
           } else if constexpr (kPreMerge) {
 #pragma unroll
             for (int c0 = 0; c0 < BNMAX; c0 += 16) {
@@ -951,9 +1078,10 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                 tmem_ld16f(tq + c0, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += pre[c0 + j];
-                store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+                emit(c0, v);
               }
             }
+            emit_end();
           } else {
             // finisher of a wide tile: own accumulator, then the partials of
             // up to four contributors at a time, in CTA order
@@ -986,8 +1114,9 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                     }
                   }
               }
-              store16(P, f, pb, ta, tb, row, c0, v, gate_s);
+              emit(c0, v);
             }
+            emit_end();
           }
           // the accumulator may be reused
           ptx::tc_fence_before();
@@ -1093,12 +1222,13 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   // (ranks up to 128); a long launch computes T once per T tile.
   P.swap = M <= kSwapMaxRows ? 1 : 0;
   int64_t wbytes = 0;
-  bool small_rank = true;
+  bool small_rank = true, any_rank = false;
   for (int p = 0; p < n; ++p) {
     wbytes += 2 * pr[p].d_in * pr[p].d_out;
     small_rank = small_rank && pr[p].rank <= kMaxLocalRank;
+    any_rank = any_rank || pr[p].rank > 0;
   }
-  P.localt = (P.swap && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
+  P.localt = (P.swap && any_rank && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
   P.out_f32 = dtype == UNO_F32;
   const int bn_tok = pick_bn(M);
 
@@ -1288,7 +1418,7 @@ cudaError_t cast_to_bf16(const void* in, void* out, int64_t n, cudaStream_t st) 
   return cudaGetLastError();
 }
 
-template <int BNMAX, bool SWAP, bool LOCALT>
+template <int BNMAX, bool SWAP, bool LOCALT, bool STATS>
 cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   static std::once_flag once[64];
   static cudaError_t attr_err[64] = {};
@@ -1296,7 +1426,7 @@ cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   cudaGetDevice(&dev);
   dev &= 63;
   std::call_once(once[dev], [&] {
-    attr_err[dev] = cudaFuncSetAttribute(grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT>,
+    attr_err[dev] = cudaFuncSetAttribute(grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT, STATS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem_bytes_for<BNMAX, LOCALT>()));
   });
@@ -1317,7 +1447,7 @@ cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT>, maps, P);
+  return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT, STATS>, maps, P);
 }
 
 }  // namespace
@@ -1392,38 +1522,89 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
   return 0;
 }
 
+namespace {
+int launch_linear(int n, const uno_lora_problem* pr, int64_t M, int dtype, void* ws,
+                  size_t ws_bytes, cudaStream_t st, const LinearEpilogue* epi);
+}  // namespace
+
 int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, void* ws,
                       size_t ws_bytes, cudaStream_t st) {
+  return launch_linear(n, pr, M, dtype, ws, ws_bytes, st, nullptr);
+}
+
+int launch_logit_gemm(const uno_lora_problem& pr, int64_t M, void* ws, size_t ws_bytes,
+                      cudaStream_t st, const LinearEpilogue& epi) {
+  return launch_linear(1, &pr, M, UNO_BF16, ws, ws_bytes, st, &epi);
+}
+
+int logit_gemm_tiles(int64_t M, int64_t d, int64_t V, int sms) {
+  uno_lora_problem p{};
+  p.d_in = d;
+  p.d_out = V;
   Layout L;
-  if (!make_layout(n, pr, M, dtype, sm_count(), L)) return UNO_ERR_ARG;
+  if (!make_layout(1, &p, M, UNO_BF16, sms, L)) return 0;
+  for (int i = 0; i < L.P.ph1[kMain]; ++i)
+    if (!L.P.ph[i].down) return int((V + (L.P.swap ? kBM : L.P.ph[i].bn) - 1) / (L.P.swap ? kBM : L.P.ph[i].bn));
+  return 0;
+}
+
+namespace {
+// The schedule and the encoded tensor maps of a launch depend only on the
+// problems' pointers and shapes, the epilogue, the workspace pointer, the
+// device and its SM count: a small per-process cache spares repeated calls
+// with the same arguments (every decode step of a serving loop) the host work
+// of building them.
+struct PlanKey {
+  int n, dtype, dev, sms, has_epi;
+  int64_t M;
+  void* ws;
+  uno_lora_problem pr[kMaxLoraProblems];
+  LinearEpilogue epi;
+};
+struct PlanEntry {
+  bool valid;
+  PlanKey key;
+  Layout L;
+  Maps maps;
+};
+constexpr int kPlanCache = 16;
+PlanEntry g_plans[kPlanCache];
+int g_plan_next = 0;
+std::mutex g_plan_mu;
+
+int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w, size_t ws_bytes,
+               int sms, const LinearEpilogue* epi, Layout& L, Maps& maps) {
+  if (!make_layout(n, pr, M, dtype, sms, L)) return UNO_ERR_ARG;
   if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
-  char* w = static_cast<char*>(ws);
   Params& P = L.P;
   P.partial = reinterpret_cast<float*>(w + L.off_partial);
   P.ready = reinterpret_cast<int*>(w + L.off_sync);
   P.tflag = P.ready + 2 * P.grid;
-  Maps maps;
   std::memset(&maps, 0, sizeof(maps));
   for (int p = 0; p < n; ++p) {
     const uno_lora_problem& q = pr[p];
     const void *x = q.x, *W = q.W, *A = q.A, *B = q.B;
-    if (dtype == UNO_F32) {
-      void* c[4];
-      for (int i = 0; i < 4; ++i) c[i] = w + L.off_cast[p][i];
-      if (cast_to_bf16(q.x, c[0], M * q.d_in, st) != cudaSuccess ||
-          cast_to_bf16(q.W, c[1], q.d_out * q.d_in, st) != cudaSuccess ||
-          (q.rank > 0 && (cast_to_bf16(q.A, c[2], q.rank * q.d_in, st) != cudaSuccess ||
-                          cast_to_bf16(q.B, c[3], q.d_out * q.rank, st) != cudaSuccess)))
-        return UNO_ERR_CUDA;
-      x = c[0];
-      W = c[1];
-      A = c[2];
-      B = c[3];
+    if (dtype == UNO_F32) {  // operands read from their bf16 copies in the workspace
+      x = w + L.off_cast[p][0];
+      W = w + L.off_cast[p][1];
+      A = w + L.off_cast[p][2];
+      B = w + L.off_cast[p][3];
     }
     Prob& b = P.pb[p];
     b.y = q.y;
     b.t = w + L.off_t[p];
     b.gate = q.gate;
+    if (epi) {
+      b.f32out = epi->f32out;
+      b.st_store = epi->stats_store;
+      b.st_K = int(epi->K);
+      b.st_Kp = int(epi->Kp);
+      b.st_Rp = int(epi->Rp);
+      b.st_nvt = epi->nvt;
+      b.st_draft = epi->draft;
+      b.st_part = epi->part;
+      b.st_gather = epi->gathered;
+    }
     int bn_main = 0, bn_down = 0;
     for (int i = 0; i < P.ph1[kMain]; ++i)
       if (P.ph[i].prob == p) (P.ph[i].down ? bn_down : bn_main) = P.ph[i].bn;
@@ -1440,6 +1621,85 @@ int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, v
     }
     if (!ok) return UNO_ERR_CUDA;
   }
+  return UNO_OK;
+}
+
+int launch_linear(int n, const uno_lora_problem* pr, int64_t M, int dtype, void* ws,
+                  size_t ws_bytes, cudaStream_t st, const LinearEpilogue* epi) {
+  char* w = static_cast<char*>(ws);
+  auto key = std::make_unique<PlanKey>();
+  std::memset(key.get(), 0, sizeof(PlanKey));
+  key->n = n;
+  key->dtype = dtype;
+  cudaGetDevice(&key->dev);
+  key->sms = sm_count();
+  key->M = M;
+  key->ws = ws;
+  for (int p = 0; p < n; ++p) {
+    uno_lora_problem& k = key->pr[p];
+    k.x = pr[p].x;
+    k.W = pr[p].W;
+    k.A = pr[p].A;
+    k.B = pr[p].B;
+    k.gate = pr[p].gate;
+    k.y = pr[p].y;
+    k.d_in = pr[p].d_in;
+    k.d_out = pr[p].d_out;
+    k.rank = pr[p].rank;
+    k.alpha = pr[p].alpha;
+  }
+  if (epi) {
+    key->has_epi = 1;
+    LinearEpilogue& e = key->epi;
+    e.f32out = epi->f32out;
+    e.stats = epi->stats;
+    e.stats_store = epi->stats_store;
+    e.K = epi->K;
+    e.Kp = epi->Kp;
+    e.Rp = epi->Rp;
+    e.nvt = epi->nvt;
+    e.draft = epi->draft;
+    e.part = epi->part;
+    e.gathered = epi->gathered;
+  }
+  auto Lp = std::make_unique<Layout>();
+  Layout& L = *Lp;
+  Maps maps;
+  bool hit = false;
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (int i = 0; i < kPlanCache && !hit; ++i)
+      if (g_plans[i].valid && std::memcmp(&g_plans[i].key, key.get(), sizeof(PlanKey)) == 0) {
+        L = g_plans[i].L;
+        maps = g_plans[i].maps;
+        hit = true;
+      }
+  }
+  if (!hit) {
+    const int rc = build_plan(n, pr, M, dtype, w, ws_bytes, key->sms, epi, L, maps);
+    if (rc != UNO_OK) return rc;
+    {
+      std::lock_guard<std::mutex> lock(g_plan_mu);
+      PlanEntry& e = g_plans[g_plan_next];
+      g_plan_next = (g_plan_next + 1) % kPlanCache;
+      e.key = *key;
+      e.L = L;
+      e.maps = maps;
+      e.valid = true;
+    }
+  }
+  if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
+  Params& P = L.P;
+  if (dtype == UNO_F32) {
+    for (int p = 0; p < n; ++p) {
+      const uno_lora_problem& q = pr[p];
+      if (cast_to_bf16(q.x, w + L.off_cast[p][0], M * q.d_in, st) != cudaSuccess ||
+          cast_to_bf16(q.W, w + L.off_cast[p][1], q.d_out * q.d_in, st) != cudaSuccess ||
+          (q.rank > 0 && (cast_to_bf16(q.A, w + L.off_cast[p][2], q.rank * q.d_in, st) != cudaSuccess ||
+                          cast_to_bf16(q.B, w + L.off_cast[p][3], q.d_out * q.rank, st) != cudaSuccess)))
+        return UNO_ERR_CUDA;
+    }
+  }
   {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(1);
@@ -1455,25 +1715,33 @@ int launch_lora_group(int n, const uno_lora_problem* pr, int64_t M, int dtype, v
       return UNO_ERR_CUDA;
   }
   cudaError_t e;
-  // one instantiation per (tile width, operand order, adapter mode)
-#define UNO_DISPATCH(SW, LT)                                             \
+  // one instantiation per (tile width, operand order, adapter mode, epilogue)
+#define UNO_DISPATCH(SW, LT, ST)                                         \
   switch (P.bnmax) {                                                     \
-    case 16: e = launch_grouped<16, SW, LT>(maps, P, st); break;         \
-    case 32: e = launch_grouped<32, SW, LT>(maps, P, st); break;         \
-    case 64: e = launch_grouped<64, SW, LT>(maps, P, st); break;         \
-    case 128: e = launch_grouped<128, SW, LT>(maps, P, st); break;       \
-    default: e = launch_grouped<256, SW, LT>(maps, P, st); break;        \
+    case 16: e = launch_grouped<16, SW, LT, ST>(maps, P, st); break;     \
+    case 32: e = launch_grouped<32, SW, LT, ST>(maps, P, st); break;     \
+    case 64: e = launch_grouped<64, SW, LT, ST>(maps, P, st); break;     \
+    case 128: e = launch_grouped<128, SW, LT, ST>(maps, P, st); break;   \
+    default: e = launch_grouped<256, SW, LT, ST>(maps, P, st); break;    \
   }
-  if (P.localt) {
-    UNO_DISPATCH(true, true)
+  if (epi && epi->stats) {
+    if (n != 1 || P.localt || pr[0].rank != 0) return UNO_ERR_UNSUPPORTED;
+    if (P.swap) {
+      UNO_DISPATCH(true, false, true)
+    } else {
+      UNO_DISPATCH(false, false, true)
+    }
+  } else if (P.localt) {
+    UNO_DISPATCH(true, true, false)
   } else if (P.swap) {
-    UNO_DISPATCH(true, false)
+    UNO_DISPATCH(true, false, false)
   } else {
-    UNO_DISPATCH(false, false)
+    UNO_DISPATCH(false, false, false)
   }
 #undef UNO_DISPATCH
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
+}  // namespace
 
 int read_device_error(int reset) {
   int v = 0;

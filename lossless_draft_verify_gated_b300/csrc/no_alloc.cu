@@ -12,7 +12,9 @@
 // cudaGetSymbolAddress, with that device current, on the first call made on that
 // device; make that first call before any stream capture.  Every call shares the
 // array: calls that may overlap on the GPU (two streams, two threads) race on it
-// and must be serialised by the caller.  The only scratch that must start at zero
+// and must be serialised by the caller.  The looked-up address belongs to the
+// device's context of the time: after cudaDeviceReset the library must not be
+// called again in the same process.  The only scratch that must start at zero
 // (the per-sequence arrival counters) is cleared by the first kernel of each call;
 // every other scratch word is written before it is read.
 #include <mutex>
@@ -56,9 +58,7 @@ int uno_verify_block_no_alloc(const float* p_logits, const float* q_logits, cons
                               int64_t K, int64_t Kp, int64_t V, int32_t* n_accepted,
                               int32_t* out_tokens, int32_t* n_emitted, int32_t* status,
                               uno_stream_t stream) {
-  if (Bn < 0 || K < 0 || K > 256 || V < 1 || V >= (int64_t(1) << 31) || (Kp != K && Kp != K + 1) ||
-      Kp < 1 || Bn > (int64_t(1) << 24))
-    return UNO_ERR_ARG;
+  if (!verify_shape_ok(Bn, K, Kp, V)) return UNO_ERR_ARG;
   if (Bn == 0) return UNO_OK;
   if (!p_logits || !u_resample || !n_accepted || !out_tokens || !n_emitted || !status)
     return UNO_ERR_ARG;

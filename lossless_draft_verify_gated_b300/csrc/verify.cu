@@ -31,9 +31,12 @@
 #include <cmath>
 
 #include "uno_internal.h"
+#include "verify_common.cuh"
 
 namespace uno {
 namespace {
+
+using namespace vfy;
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -46,44 +49,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;  // float4 loads in flight per thread in the statistics pass
 constexpr int kRace = 0, kInverseCdf = 1;  // resample modes (uno.h: UNO_RESAMPLE_*)
-
-struct MS {
-  float m, s;  // running max and sum of exp(x - m)
-};
-
-__device__ __forceinline__ MS ms_merge(MS a, MS b) {
-  const float m = fmaxf(a.m, b.m);
-  if (m == -INFINITY) return {m, a.s + b.s};
-  return {m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
-}
-
-// Fold four logits into a running (max, sum).  NaN poisons s; +inf makes
-// s NaN through inf - inf; -inf entries contribute exactly 0.
-__device__ __forceinline__ void ms_add4(MS& a, float x0, float x1, float x2, float x3) {
-  const float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-  if (mx > a.m) {
-    a.s *= __expf(a.m - mx);
-    a.m = mx;
-  }
-  if (a.m != -INFINITY) {
-    a.s += __expf(x0 - a.m) + __expf(x1 - a.m) + __expf(x2 - a.m) + __expf(x3 - a.m);
-  } else if (isnan(x0) || isnan(x1) || isnan(x2) || isnan(x3)) {
-    a.s = NAN;
-  }
-}
-
-__device__ __forceinline__ void ms_add1(MS& a, float x) {
-  ms_add4(a, x, -INFINITY, -INFINITY, -INFINITY);
-}
-
-__device__ __forceinline__ MS warp_merge(MS a) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MS b{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
-    a = ms_merge(a, b);
-  }
-  return a;
-}
 
 // Row j of sequence b: j < Kp is AR row j, else draft row j - Kp.
 __device__ __forceinline__ const float* row_ptr(const float* p, const float* q, int64_t b,
@@ -171,34 +136,6 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
     part[unit] = make_float2(t.m, t.s);
   }
 }
-
-struct Cand {
-  float s;  // race score
-  int v;    // vocab id, -1 = none
-};
-
-__device__ __forceinline__ Cand cand_best(Cand a, Cand b) {
-  if (b.s > a.s || (b.s == a.s && b.v >= 0 && (a.v < 0 || b.v < a.v))) return b;
-  return a;
-}
-
-__device__ __forceinline__ Cand warp_best(Cand a) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Cand b{__shfl_xor_sync(0xffffffffu, a.s, o), __shfl_xor_sync(0xffffffffu, a.v, o)};
-    a = cand_best(a, b);
-  }
-  return a;
-}
-
-struct RacePart {
-  float sr;  // best residual score in the chunk (0 if no positive residual)
-  int vr;
-  float sp;  // best score of the AR row itself (fallback and bonus race)
-  int vp;
-};
-// (inverse CDF) the same slot holds the chunk's residual and AR weight sums
-static_assert(sizeof(RacePart) == sizeof(longlong2), "chunk sums share the race slot");
 
 constexpr int kMaxRows = 2 * 256 + 1;  // Kp + K rows of one sequence held in smem
 
@@ -658,6 +595,9 @@ VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   pl.off_race = align_up(pl.off_gather + size_t(pl.rows) * sizeof(float), 256);
   pl.off_count = align_up(pl.off_race + size_t(Bn) * pl.race_splits * sizeof(RacePart), 256);
   pl.bytes = align_up(pl.off_count + size_t(Bn) * sizeof(int), 256);
+  // the one-launch path for small batches shares the workspace
+  plan_verify_fused(Bn, K, Kp, V, sms, pl);
+  if (pl.fused) pl.bytes = std::max(pl.bytes, pl.fused_bytes);
   return pl;
 }
 
@@ -666,31 +606,69 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                           int64_t Kp, int64_t V, int32_t* n_acc, int32_t* out_tokens,
                           int32_t* n_emit, int32_t* status, void* ws, const VerifyPlan& pl,
                           cudaStream_t st, float inv_t, int mode) {
+  const bool ex = inv_t != 1.0f || mode != kRace;
+  const uintptr_t rows_addr = reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q) |
+                              reinterpret_cast<uintptr_t>(u_res);
+  if (pl.fused && !ex && (rows_addr & 15u) == 0) {
+    // small batch: one cooperative launch (falls back if the device cannot
+    // hold one CTA per SM of it)
+    const cudaError_t e = launch_verify_fused(p, q, draft, u_acc, u_res, Bn, K, Kp, V, n_acc,
+                                              out_tokens, n_emit, status, ws, pl, st);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    cudaGetLastError();
+  }
   char* w = static_cast<char*>(ws);
   float2* part = reinterpret_cast<float2*>(w + pl.off_stats);
   float* gathered = reinterpret_cast<float*>(w + pl.off_gather);
   RacePart* rpart = reinterpret_cast<RacePart*>(w + pl.off_race);
   int* counter = reinterpret_cast<int*>(w + pl.off_count);
   const int64_t g1 = pl.rows * pl.splits;
-  const bool ex = inv_t != 1.0f || mode != kRace;
-  if (ex)
-    verify_stats_kernel<true><<<dim3(unsigned(g1)), kThreads, 0, st>>>(
-        p, q, draft, K, Kp, V, pl.splits, pl.chunk, inv_t, part, gathered, counter);
-  else
-    verify_stats_kernel<false><<<dim3(unsigned(g1)), kThreads, 0, st>>>(
-        p, q, draft, K, Kp, V, pl.splits, pl.chunk, inv_t, part, gathered, counter);
-  cudaError_t e = cudaGetLastError();
+  // Both kernels are launched with programmatic stream serialization: each
+  // may start while the launch before it drains, and waits for it
+  // (griddepcontrol.wait) before it reads anything that launch writes.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(unsigned(g1));
+  cudaError_t e = ex ? cudaLaunchKernelEx(&cfg, verify_stats_kernel<true>, p, q, draft, K, Kp, V,
+                                          pl.splits, pl.chunk, inv_t, part, gathered, counter)
+                     : cudaLaunchKernelEx(&cfg, verify_stats_kernel<false>, p, q, draft, K, Kp, V,
+                                          pl.splits, pl.chunk, inv_t, part, gathered, counter);
   if (e != cudaSuccess) return e;
-  const int64_t g2 = Bn * pl.race_splits;
-  if (ex)
-    verify_finish_kernel<true><<<dim3(unsigned(g2)), kThreads, 0, st>>>(
-        p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
-        part, gathered, rpart, counter, n_acc, out_tokens, n_emit, status);
-  else
-    verify_finish_kernel<false><<<dim3(unsigned(g2)), kThreads, 0, st>>>(
-        p, q, draft, u_acc, u_res, K, Kp, V, pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
-        part, gathered, rpart, counter, n_acc, out_tokens, n_emit, status);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(unsigned(Bn * pl.race_splits));
+  e = ex ? cudaLaunchKernelEx(&cfg, verify_finish_kernel<true>, p, q, draft, u_acc, u_res, K, Kp, V,
+                              pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
+                              (const float2*)part, (const float*)gathered, rpart, counter, n_acc,
+                              out_tokens, n_emit, status)
+         : cudaLaunchKernelEx(&cfg, verify_finish_kernel<false>, p, q, draft, u_acc, u_res, K, Kp,
+                              V, pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
+                              (const float2*)part, (const float*)gathered, rpart, counter, n_acc,
+                              out_tokens, n_emit, status);
+  return e;
+}
+
+cudaError_t launch_row_stats(const float* p, const float* q, const int32_t* draft, int64_t Bn,
+                             int64_t K, int64_t Kp, int64_t V, const VerifyPlan& pl, void* ws,
+                             cudaStream_t st) {
+  char* w = static_cast<char*>(ws);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(unsigned(pl.rows * pl.splits));
+  return cudaLaunchKernelEx(&cfg, verify_stats_kernel<false>, p, q, draft, K, Kp, V, pl.splits,
+                            pl.chunk, 1.0f, reinterpret_cast<float2*>(w + pl.off_stats),
+                            reinterpret_cast<float*>(w + pl.off_gather),
+                            reinterpret_cast<int*>(w + pl.off_count));
 }
 
 cudaError_t launch_draft_sample(const float* logits, const float* u, int64_t R, int64_t V,

@@ -156,3 +156,34 @@ def verify_problem(Bn: int, K: int, V: int, *, Kp: int | None = None, sigma: flo
     ud = (uniform_race((Bn, K, V), f"verify.ud.{tag}", seed, device) if with_u_draft
           else torch.empty(0, device=device))
     return VerifyProblem(p, q, ua, ur, ud)
+
+
+@dataclass
+class LmHeadProblem:
+    h: torch.Tensor           # [Bn*Kp + Bn*K, d] bf16: AR rows of every sequence, then draft rows
+    W: torch.Tensor           # [V, d] bf16 LM head
+    u_accept: torch.Tensor    # [Bn, K]
+    u_resample: torch.Tensor  # [Bn, V]
+    u_draft: torch.Tensor     # [Bn, K, V]
+    Bn: int
+    K: int
+    Kp: int
+
+
+def lm_head_problem(Bn: int, K: int, V: int, d: int, *, Kp: int | None = None, sigma: float = 1.0,
+                    logit_std: float = 3.0, seed: int = BASE_SEED, device="cpu") -> LmHeadProblem:
+    """Final hidden states and an LM head whose logits have the verifier's
+    workload statistics: AR hidden states ~ N(0, 1), W ~ N(0, logit_std/sqrt(d))
+    (logits ~ N(0, logit_std)); the draft rows' hidden states are the AR rows'
+    plus N(0, sigma/logit_std), so draft logits are AR logits plus about
+    N(0, sigma)."""
+    Kp = K if Kp is None else Kp
+    tag = f"B{Bn}.K{K}.Kp{Kp}.V{V}.d{d}.s{sigma}"
+    ha = normal((Bn, Kp, d), 1.0, f"lm.ha.{tag}", seed, torch.float32, device)
+    hd = ha[:, :K] + normal((Bn, K, d), sigma / logit_std, f"lm.hd.{tag}", seed, torch.float32, device)
+    h = torch.cat([ha.reshape(Bn * Kp, d), hd.reshape(Bn * K, d)]).to(torch.bfloat16)
+    W = normal((V, d), logit_std / d ** 0.5, f"lm.W.V{V}.d{d}", seed, torch.bfloat16, device)
+    ua = uniform_accept((Bn, K), f"lm.ua.{tag}", seed, device)
+    ur = uniform_race((Bn, V), f"lm.ur.{tag}", seed, device)
+    ud = uniform_race((Bn, K, V), f"lm.ud.{tag}", seed, device)
+    return LmHeadProblem(h, W, ua, ur, ud, Bn, K, Kp)

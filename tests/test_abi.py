@@ -155,3 +155,57 @@ def test_batched_argument_errors(L):
     w1 = binding.uno_gated_lora_linear_batched_workspace([(4096, 4096, 128)] * 7, 32, 1)
     w2 = binding.uno_gated_lora_linear_workspace(32, 4096, 4096, 128, 1)
     assert w1 > w2 > 0
+
+
+def test_tree_argument_errors(L):
+    """uno_tree_verify: sizes, nulls, alignment and workspace checked on the host."""
+    from lossless_draft_verify_gated_b300 import binding
+    P = ctypes.c_void_p
+    ins = [P(256)] * 5
+    outs = [P(256)] * 5
+
+    def call(Bn=2, N=4, V=100, ws=P(256), ws_bytes=1 << 20, l0=None, path=P(256)):
+        ii = list(ins)
+        if l0 is not None:
+            ii[0] = l0
+        oo = list(outs)
+        oo[1] = path
+        return L.uno_tree_verify(*ii, Bn, N, V, *oo, ws, ws_bytes, None)
+
+    assert call(N=256) == -1 and call(N=-1) == -1 and call(V=0) == -1
+    assert call(l0=P(0)) == -1
+    assert call(path=None) == -1
+    assert call(l0=P(258)) == -2
+    assert call(ws=P(264)) == -4
+    assert call(ws_bytes=8) == -4
+    assert call(Bn=0) == 0
+    w = binding.uno_tree_verify_workspace(4, 30, 128256)
+    assert w > 0 and w % 256 == 0
+    assert binding.uno_tree_verify_workspace(4, 256, 128256) == 0
+
+
+def test_lm_head_argument_errors(L):
+    """uno_lm_head_verify: mode, sizes (d and V multiples of 8), nulls,
+    16-byte alignment of h, W and u_resample, workspace."""
+    from lossless_draft_verify_gated_b300 import binding
+    P = ctypes.c_void_p
+    outs = [P(256)] * 4
+
+    def call(Bn=2, K=4, Kp=4, V=1000, d=256, mode=0, h=P(256), W=P(256), ws=P(256),
+             ws_bytes=1 << 30):
+        return L.uno_lm_head_verify(h, W, P(256), P(256), P(256), Bn, K, Kp, V, d, mode, *outs, ws,
+                                    ws_bytes, None)
+
+    assert call(mode=4) == -1 and call(mode=-1) == -1
+    assert call(V=1001) == -1 and call(d=100) == -1 and call(Kp=6) == -1
+    assert call(h=None) == -1
+    assert call(h=P(264)) == -2 and call(W=P(8)) == -2
+    assert call(ws=P(264)) == -4 and call(ws_bytes=16) == -4
+    assert call(Bn=0) == 0
+    for mode in ("auto", "plain", "stats_store", "stats_recompute"):
+        w = binding.uno_lm_head_verify_workspace(256, 16, 16, 128256, 4096, mode)
+        assert w > 0 and w % 256 == 0
+    # storing the logits takes 4 bytes per logit; recomputing the resampled rows does not
+    big = binding.uno_lm_head_verify_workspace(256, 16, 16, 128256, 4096, "stats_store")
+    small = binding.uno_lm_head_verify_workspace(256, 16, 16, 128256, 4096, "stats_recompute")
+    assert big > 256 * 32 * 128256 * 4 > small

@@ -57,6 +57,47 @@ def test_verify_parity_full_size(sigma):
     assert mean_em >= 1.0
 
 
+@pytest.mark.parametrize("Bn", [1, 8, 32, 128, 512])
+def test_verify_parity_step_sweep(Bn):
+    """The verifier of the benchmarked step at every batch of the sweep
+    (block 16, vocab 128256, sigma 1), each with its own launch plan (at batch
+    1 the statistics pass splits every row 37 ways and the race 126 ways);
+    every sequence against the oracle."""
+    ref, gpu, ties = _run_case(Bn, 16, 128256, None, 1.0)
+    assert gpu[2].sum().item() >= Bn
+
+
+def _shifted(t):
+    """A contiguous copy of t whose data start 4 bytes past a 16-byte boundary
+    (rows stay 4-byte aligned): the verifier then takes its two-launch path."""
+    buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 == 4
+    return v
+
+
+@pytest.mark.parametrize("Bn,K,V,Kp", [(1, 16, 128256, None), (3, 16, 128256, 17),
+                                       (16, 16, 128256, None), (5, 7, 1000, 8), (16, 4, 64, None)])
+def test_one_launch_and_two_launch_paths(Bn, K, V, Kp):
+    """Small batches with a vocabulary divisible by 4 and 16-byte aligned rows
+    take the one-launch verifier; the same inputs 4 bytes off alignment take
+    the two-launch kernels.  Both match the oracle."""
+    from lossless_draft_verify_gated_b300 import uno_device_error, uno_verify_block
+    pr = inputs.verify_problem(Bn, K, V, Kp=Kp, sigma=1.0, seed=77)
+    draft, st, _ = oracle.draft_sample(pr.q_logits, pr.u_draft)
+    draft = draft.reshape(Bn, K)
+    ref = oracle.verify_block(pr.p_logits, pr.q_logits, draft, pr.u_accept, pr.u_resample)
+    args = [pr.p_logits.cuda(), pr.q_logits.cuda(), torch.from_numpy(draft).cuda(),
+            pr.u_accept.cuda(), pr.u_resample.cuda()]
+    one = uno_verify_block(*args)
+    two = uno_verify_block(_shifted(args[0]), _shifted(args[1]), args[2], args[3], _shifted(args[4]))
+    torch.cuda.synchronize()
+    compare_verify(one, ref, Bn)
+    compare_verify(two, ref, Bn)
+    assert uno_device_error() == 0
+
+
 def test_q_equals_p_accepts_all():
     from lossless_draft_verify_gated_b300 import uno_verify_block
     Bn, K, V = 33, 8, 5000
