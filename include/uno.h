@@ -294,7 +294,9 @@ int uno_verify_block_no_alloc(const float *p_logits, const float *q_logits,
  *              UNO_LM_STATS_RECOMPUTE: the epilogue leaves only the
  *                statistics (no logit reaches memory); the two rows per
  *                sequence that the resample needs are recomputed;
- *              UNO_LM_AUTO: one of the two statistics modes by batch size.
+ *              UNO_LM_AUTO: PLAIN below 8 sequences, STATS_STORE from 8
+ *                (the fastest on a B300; STATS_RECOMPUTE needs no logit
+ *                buffer, the choice where workspace memory is short).
  *              All modes compute the same function (bf16 operands, fp32
  *              accumulation; they may differ in the last bits of a logit).
  *   workspace  at least uno_lm_head_verify_workspace(Bn, K, Kp, V, d, mode)

@@ -432,9 +432,15 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
     const float gs = f.down ? float(pb.gate[m]) * pb.scale : 1.f;
     if (!f.down && (P.out_f32 || pb.f32out)) {
       float* d = static_cast<float*>(pb.y) + int64_t(m) * ncols;
+      if (n0 + 16 <= ncols) {  // ncols and n0 are multiples of 8: 16-byte stores
+        float4* d4 = reinterpret_cast<float4*>(d + n0);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (n0 + j < ncols) d[n0 + j] = v[j];
+        for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (n0 + j < ncols) d[n0 + j] = v[j];
+      }
     } else if (n0 + 16 <= ncols) {
       uint32_t w[8];
 #pragma unroll

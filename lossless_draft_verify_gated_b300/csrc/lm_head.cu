@@ -284,9 +284,7 @@ cudaLaunchConfig_t pdl_config(dim3 grid, cudaStream_t st, cudaLaunchAttribute* a
 
 LmPlan plan_lm_head(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int64_t d, int mode, int sms) {
   LmPlan L{};
-  L.mode = mode == UNO_LM_AUTO ? (Bn >= kLmRecomputeMinBatch ? UNO_LM_STATS_RECOMPUTE
-                                                             : UNO_LM_STATS_STORE)
-                               : mode;
+  L.mode = mode == UNO_LM_AUTO ? (Bn >= kLmStatsMinBatch ? UNO_LM_STATS_STORE : UNO_LM_PLAIN) : mode;
   L.rows = Bn * (Kp + K);
   uno_lora_problem p{};
   p.d_in = d;

@@ -203,20 +203,33 @@ tree_finish_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   float pn = -1.f, pd = 1.f, rn = 0.f, rd = 1.f;
   int pvid = -1, rvid = -1;
   int ptr = 0;  // first rejected token >= v (v grows along this thread's loop)
-  for (int64_t v = v0 + tid; v < v1; v += kTT) {
-    const float e = -logf(ub[v]);
-    const float pv = exp2f((pr[v] - mp) * kLog2e) * izp;
-    while (ptr < nrej && s_rej[ptr] < v) ++ptr;
-    const bool rejected = ptr < nrej && s_rej[ptr] == v;
-    if (pv * pd > pn * e) {  // pv / e > pn / pd; ties keep the lower id
-      pn = pv;
-      pd = e;
-      pvid = int(v);
+  constexpr int kU = 4;  // loads in flight per thread
+  for (int64_t v0t = v0 + tid; v0t < v1; v0t += int64_t(kTT) * kU) {
+    float uu[kU], lp[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int64_t v = v0t + int64_t(k) * kTT;
+      uu[k] = v < v1 ? ub[v] : 0.5f;
+      lp[k] = v < v1 ? pr[v] : -INFINITY;
     }
-    if (!rejected && pv > 0.f && pv * rd > rn * e) {
-      rn = pv;
-      rd = e;
-      rvid = int(v);
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int64_t v = v0t + int64_t(k) * kTT;
+      if (v >= v1) break;
+      const float e = -logf(uu[k]);
+      const float pv = exp2f((lp[k] - mp) * kLog2e) * izp;
+      while (ptr < nrej && s_rej[ptr] < v) ++ptr;
+      const bool rejected = ptr < nrej && s_rej[ptr] == v;
+      if (pv * pd > pn * e) {  // pv / e > pn / pd; ties keep the lower id
+        pn = pv;
+        pd = e;
+        pvid = int(v);
+      }
+      if (!rejected && pv > 0.f && pv * rd > rn * e) {
+        rn = pv;
+        rd = e;
+        rvid = int(v);
+      }
     }
   }
   Cand cr{rvid >= 0 ? rn / rd : 0.f, rvid}, cp{pvid >= 0 ? pn / pd : -1.f, pvid};
@@ -246,13 +259,29 @@ tree_finish_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   __syncthreads();
   if (!s_last) return;
   if (race_splits > 1) {
+    // merge every chunk's winners: loads spread over the block, then the warp
+    // and block reductions
     __threadfence();
+    Cand br{0.f, -1}, bp{-1.f, -1};
+    for (int s = tid; s < race_splits; s += kTT) {
+      const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
+      br = cand_best(br, Cand{__int_as_float(t.x), t.y});
+      bp = cand_best(bp, Cand{__int_as_float(t.z), t.w});
+    }
+    br = warp_best(br);
+    bp = warp_best(bp);
+    __syncthreads();
+    if (lane == 0) {
+      s_cr[warp] = br;
+      s_cp[warp] = bp;
+    }
+    __syncthreads();
     if (tid == 0) {
-      Cand br{0.f, -1}, bp{-1.f, -1};
-      for (int s = 0; s < race_splits; ++s) {
-        const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
-        br = cand_best(br, Cand{__int_as_float(t.x), t.y});
-        bp = cand_best(bp, Cand{__int_as_float(t.z), t.w});
+      br = s_cr[0];
+      bp = s_cp[0];
+      for (int w = 1; w < kTW; ++w) {
+        br = cand_best(br, s_cr[w]);
+        bp = cand_best(bp, s_cp[w]);
       }
       s_tok_out = br.v >= 0 ? br.v : bp.v;
       counter[b] = 0;

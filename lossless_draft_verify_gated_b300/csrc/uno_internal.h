@@ -23,8 +23,9 @@ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) & ~(a - 1); }
 // Kp in {K, K+1} with Kp >= 1, 1 <= V < 2^31, 0 <= Bn <= 2^24.
 bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V);
 
-// Largest batch the one-launch verifier (verify_fused.cu) takes.
-constexpr int64_t kFusedMaxBatch = 16;
+// Largest batch the one-launch verifier (verify_fused.cu) takes: at batch 1 it
+// matches the two launches (about 29 us on a B300), above it they are faster.
+constexpr int64_t kFusedMaxBatch = 1;
 
 struct VerifyPlan {
   int64_t rows;      // Bn * (Kp + K): AR rows then draft rows of each sequence
@@ -104,9 +105,11 @@ int launch_logit_gemm(const uno_lora_problem& pr, int64_t M, void* ws, size_t ws
 int logit_gemm_tiles(int64_t M, int64_t d, int64_t V, int sms);
 
 // -------------------------------------------------------------- LM head
-// Batches from which UNO_LM_AUTO recomputes the raced rows instead of storing
-// every logit row.
-constexpr int64_t kLmRecomputeMinBatch = 64;
+// Batches from which UNO_LM_AUTO takes the verifier's statistics in the head
+// GEMM's epilogue (the logits are still stored, which the tensor-bound GEMM
+// hides, and only the resampled rows are read back); below it, where the
+// head's weights dominate the traffic, the plain path is as fast.
+constexpr int64_t kLmStatsMinBatch = 8;
 
 struct LmPlan {
   int mode;          // UNO_LM_PLAIN, UNO_LM_STATS_STORE or UNO_LM_STATS_RECOMPUTE

@@ -53,6 +53,7 @@ constexpr uint32_t kFRingBytes = uint32_t(kFStages) * kFChunk * 4;
 constexpr uint64_t kFWaitNs = 1000000000ull;  // 1 s: the barrier's partners are co-resident
 constexpr int kFMaxG = 160;    // CTAs of the launch (one per SM)
 constexpr int kFRaceUnroll = 4;
+constexpr int kFMaxRowsPerSlice = 64;  // rows whose drafted token a CTA keeps in shared memory
 
 struct FusedArgs {
   const float* p;         // [Bn, Kp, V]
@@ -146,6 +147,15 @@ __global__ void __launch_bounds__(kFT, 1) verify_fused_kernel(const __grid_const
   const int64_t V = a.V, K = a.K, Kp = a.Kp, Bn = a.Bn;
   const int64_t e0 = c < a.Gs ? a.sstart[c] : 0, e1 = c < a.Gs ? a.sstart[c + 1] : 0;
 
+  // Inputs read before anything else: the drafted token of every row this
+  // CTA streams, and this thread's accept inputs of step 2.
+  __shared__ int32_t s_xd[kFMaxRowsPerSlice];
+  const int64_t row0 = e0 / V;
+  const int nrows = e0 < e1 ? int(min(int64_t(kFMaxRowsPerSlice), (e1 - 1) / V - row0 + 1)) : 0;
+  if (tid < nrows) s_xd[tid] = int32_t(row_draft(a, row0 + tid));
+  // (the first of this thread's accept tests; any further ones load in step 2)
+  const int32_t x_pre = tid < Bn * K ? a.draft[tid] : 0;
+  const float u_pre = tid < Bn * K ? a.u_acc[tid] : 0.f;
   if (tid == 0) {
     for (int s = 0; s < kFStages; ++s) ptx::mbar_init(&full[s], 1);
     ptx::fence_mbar_init();
@@ -199,17 +209,23 @@ __global__ void __launch_bounds__(kFT, 1) verify_fused_kernel(const __grid_const
     __syncthreads();
     acc = MS{-INFINITY, 0.f};
   };
-  int64_t xd = e0 < e1 ? row_draft(a, cur_row) : -1;
+  auto draft_of = [&](int64_t r) -> int64_t {
+    return r - row0 < kFMaxRowsPerSlice ? int64_t(s_xd[r - row0]) : row_draft(a, r);
+  };
+  int64_t xd = e0 < e1 ? draft_of(cur_row) : -1;
   uint32_t i = 0;
   for (; ck.cur < e1; ++i) {
     const int64_t len = ck.len();
     if (ck.row != cur_row) {
       flush_row();
       cur_row = ck.row;
-      xd = row_draft(a, cur_row);
+      xd = draft_of(cur_row);
     }
     const int slot = int(i % kFStages);
-    if (!ptx::mbar_wait(&full[slot], (i / kFStages) & 1, kFWaitNs)) s_timeout = 1;
+    // one thread waits for the stage (many threads polling the barrier slow
+    // the copies landing in the same shared memory), then releases the block
+    if (tid == 0 && !ptx::mbar_wait(&full[slot], (i / kFStages) & 1, kFWaitNs)) s_timeout = 1;
+    __syncthreads();
     const int64_t v0 = ck.cur - cur_row * V;
     const float4* st4 = reinterpret_cast<const float4*>(ring + size_t(slot) * kFChunk);
     const int n4 = int(len >> 2);
@@ -279,26 +295,28 @@ __global__ void __launch_bounds__(kFT, 1) verify_fused_kernel(const __grid_const
     s_bad[b] = 0;
   }
   __syncthreads();
-  for (int64_t r = warp; r < R; r += kFW) {
+  // one thread per row, its slots merged in slot order (loads of many rows in flight)
+  for (int64_t r = tid; r < R; r += kFT) {
     MS t{-INFINITY, 0.f};
-    for (int k = lane; k < a.S; k += 32) {
-      const float2 v = __ldcg(a.part + r * a.S + k);
-      t = ms_merge(t, MS{v.x, v.y});
+    for (int k0 = 0; k0 < a.S; k0 += 8) {
+      float2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = k0 + k < a.S ? __ldcg(a.part + r * a.S + k0 + k) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t = ms_merge(t, MS{v[k].x, v[k].y});
     }
-    t = warp_merge(t);
-    if (lane == 0) {
-      const int64_t b = r < Rp ? r / Kp : (r - Rp) / K;
-      const bool bad = isnan(t.s) || !(t.m > -INFINITY) || !(t.m < INFINITY) || !(t.s > 0.f);
-      if (bad) atomicOr(&s_bad[b], 2);
-      s_m[r] = t.m;
-      s_lz[r] = t.m + logf(t.s);
-      s_iz[r] = 1.0f / t.s;
-    }
+    const int64_t b = r < Rp ? r / Kp : (r - Rp) / K;
+    const bool bad = isnan(t.s) || !(t.m > -INFINITY) || !(t.m < INFINITY) || !(t.s > 0.f);
+    if (bad) atomicOr(&s_bad[b], 2);
+    s_m[r] = t.m;
+    s_lz[r] = t.m + logf(t.s);
+    s_iz[r] = 1.0f / t.s;
   }
   __syncthreads();
   for (int64_t t = tid; t < Bn * K; t += kFT) {
     const int64_t b = t / K, i2 = t - b * K;
-    const int32_t x = a.draft[t];
+    const int32_t x = t == tid ? x_pre : a.draft[t];
     if (x < 0 || x >= V) {
       atomicOr(&s_bad[b], 1);
       continue;
@@ -311,7 +329,7 @@ __global__ void __launch_bounds__(kFT, 1) verify_fused_kernel(const __grid_const
     } else {
       const float lp = __ldcg(a.gathered + b * Kp + i2);
       const float lr = (lp - s_lz[b * Kp + i2]) - (lq - s_lz[Rp + t]);
-      accept = a.u_acc[t] < fminf(1.0f, expf(lr));
+      accept = (t == tid ? u_pre : a.u_acc[t]) < fminf(1.0f, expf(lr));
     }
     if (!accept) atomicMin(&s_n[b], int(i2));
   }

@@ -187,3 +187,38 @@ def test_gpu_tree_losslessness_chi_square():
         assert np.array_equal(sel, first == tok[c])
         obs = np.bincount(toks[sel, 1], minlength=V)
         assert stats.chisquare(obs, P[c] * sel.sum()).pvalue > 1e-3, c
+
+
+def test_chain_equals_linear_verifier_on_gpu():
+    """On the GPU as in the oracle: a chain tree verifies exactly like the
+    linear block verifier whose draft distributions are one-hot at the drafted
+    tokens (a point-mass draft), bonus row included."""
+    from lossless_draft_verify_gated_b300 import uno_tree_verify, uno_verify_block
+    rng = np.random.default_rng(17)
+    Bn, K, V = 64, 8, 128256
+    lp = (rng.standard_normal((Bn, K + 1, V)) * 8).astype(np.float32)
+    draft = np.where(rng.random((Bn, K)) < 0.85, np.argmax(lp[:, :K], axis=2),
+                     rng.integers(0, V, (Bn, K))).astype(np.int32)
+    q = np.full((Bn, K, V), -np.inf, np.float32)
+    np.put_along_axis(q, draft[:, :, None], 0.0, axis=2)
+    ua = _ua(rng, (Bn, K))
+    ur = _ur(rng, (Bn, V))
+    d = "cuda"
+    lin = uno_verify_block(torch.from_numpy(lp).to(d), torch.from_numpy(q).to(d),
+                           torch.from_numpy(draft).to(d), torch.from_numpy(ua).to(d),
+                           torch.from_numpy(ur).to(d))
+    par = np.tile(np.arange(-1, K, dtype=np.int32), (Bn, 1))
+    tok = np.concatenate([np.zeros((Bn, 1), np.int32), draft], axis=1)
+    ua_t = np.concatenate([np.zeros((Bn, 1), np.float32), ua], axis=1)
+    tr = uno_tree_verify(torch.from_numpy(lp).to(d), torch.from_numpy(par).to(d),
+                         torch.from_numpy(tok).to(d), torch.from_numpy(ua_t).to(d),
+                         torch.from_numpy(ur).to(d))
+    torch.cuda.synchronize()
+    # both sides decide in fp32: compare outside the oracle's near ties
+    ref = oracle.tree_verify(lp, par, tok, ua_t, ur)
+    keep = ~((ref.accept_margin < NEAR_TIE).any(axis=1) | (ref.race_margin < NEAR_TIE))
+    n_lin, t_lin = lin[0].cpu().numpy(), lin[1].cpu().numpy()
+    n_tr, t_tr = tr[0].cpu().numpy(), tr[2].cpu().numpy()
+    np.testing.assert_array_equal(n_lin[keep], n_tr[keep])
+    np.testing.assert_array_equal(t_lin[keep], t_tr[keep, :K + 1])
+    assert (n_lin == K).any() and (n_lin < K).any()
