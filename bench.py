@@ -52,6 +52,14 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the batch sweep (batch 1-512) and the verifier sigma sweep")
     ap.add_argument("--sweep-steps", type=int, default=20, help="timed steps per sweep point")
+    ap.add_argument("--profile", choices=["lm_head", "tree"], default=None,
+                    help="replay one op a few times for a profiler (no JSON line): the LM head + "
+                         "verifier (--batch, --lm-mode) or the tree sampler (--batch)")
+    ap.add_argument("--lm-mode", choices=["plain", "stats_store", "stats_recompute"], default="stats_recompute")
+    ap.add_argument("--l2-flush", choices=["write", "write_read"], default="write_read",
+                    help="L2 flush before every step, outside the timed events: a write of twice "
+                         "the L2 size, then (write_read) a read of another such buffer, so that the "
+                         "step does not start by writing back the flush's own dirty lines")
     ap.add_argument("--no-graph", action="store_true", help="launch ops eagerly instead of replaying a CUDA graph")
     ap.add_argument("--temperature", type=float, default=1.0,
                     help="sampling temperature of the verifier (drafts drawn from q at the same T)")
@@ -131,7 +139,7 @@ def verify_bytes(batch, n_race, resample="race"):
     """p and q once, drafts and accept uniforms, and the resample's uniforms:
     a vocabulary row per race, one value per sequence for the inverse CDF."""
     u = 4 * VOCAB * n_race if resample == "race" else 4 * batch
-    return 8 * batch * BLOCK * VOCAB + 12 * batch * BLOCK + u
+    return int(round(8 * batch * BLOCK * VOCAB + 12 * batch * BLOCK + u))
 
 
 class Clocks:
@@ -206,10 +214,10 @@ def aggregate(ms_step, tokens, ws, device):
     import torch
     import torch.distributed as dist
     t = torch.tensor([ms_step], dtype=torch.float64, device=device)
-    n = torch.tensor([tokens], dtype=torch.int64, device=device)
+    n = torch.tensor([tokens], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(n, op=dist.ReduceOp.SUM)
-    return float(t.item()), int(n.item())
+    return float(t.item()), float(n.item())
 
 
 GROUPINGS = {"layer": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
@@ -219,6 +227,10 @@ GROUPINGS = {"layer": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
 SWEEP_BATCHES = (1, 8, 32, 128, 512)   # full step at batch 1-512 (M = 32 x batch)
 SWEEP_SIGMAS = (0.25, 1.0, 4.0)        # verifier alone at batch 256, acceptance high to low
 SWEEP_VERIFY_BATCH = 256
+VERIFY_SET_SEQS = 64                   # a step at batch B cycles through 64 // B verifier input sets
+LM_D = 4096                            # Llama-3-8B hidden size: the LM head is [128256, 4096]
+SWEEP_LM_BATCHES = (1, 256)
+SWEEP_TREE = ((1, (3, 2, 2, 1)), (8, (3, 2, 2, 1)))  # (batch, children per node at each depth)
 
 
 def config_dict(args, batch, ws):
@@ -228,7 +240,8 @@ def config_dict(args, batch, ws):
             "rows_per_projection": 2 * BLOCK * batch,
             "grouping": args.grouping + ": " + " | ".join(",".join(g) for g in GROUPINGS[args.grouping]),
             "sampler": f"temperature {args.temperature}, {args.resample} resample",
-            "l2": "flushed before every step (2x L2 write, outside the timed events)",
+            "l2": ("flushed before every step, outside the timed events: a 2x L2 write" +
+                   (", then a 2x L2 read of another buffer" if args.l2_flush == "write_read" else "")),
             "parallelism": f"dp{ws} (independent replicas, no collective)"}
 
 
@@ -267,24 +280,36 @@ class Step:
                                  dtype=torch.uint8, device=device)
                 self.groups.append((probs, ws))
             self.n_gate1 = int(self.layer[0][1].gate.sum())
-        vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=gen_dev)
-        if host_inputs:
-            vp = inputs.VerifyProblem(*(t.to(device) for t in (vp.p_logits, vp.q_logits, vp.u_accept,
-                                                               vp.u_resample, vp.u_draft)))
-        self.p, self.q, self.ua, self.ur = vp.p_logits, vp.q_logits, vp.u_accept, vp.u_resample
         self.temperature, self.resample = temperature, resample
         self.plain = temperature == 1.0 and resample == "race"
-        if resample == "inverse_cdf":  # one uniform per sequence
-            self.ur = inputs.uniform_accept((batch,), f"verify.u1.B{batch}", device=device)
-        # drafts: the linear sampler's drafting half, a single token drawn from q (at the
-        # verifier's temperature) at each position
-        qd = self.q if temperature == 1.0 else (self.q.double() / temperature).float()
-        self.draft, st = binding.uno_draft_sample(qd, vp.u_draft)
-        del qd
-        assert int(st.abs().sum()) == 0
-        del vp
-        self.vout = tuple(torch.empty(s, dtype=torch.int32, device=device)
-                          for s in [(batch,), (batch, BLOCK + 1), (batch,), (batch,)])
+        # Verifier inputs: at a small batch the accepted lengths of a single draw
+        # say little about the mean, so consecutive steps cycle through several
+        # seeded input sets (at least VERIFY_SET_SEQS sequences in all).  Set 0
+        # is the one drawn as host_inputs asks (the one the oracle sample reads).
+        self.vsets = []
+        for k in range(max(1, VERIFY_SET_SEQS // batch)):
+            vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=gen_dev if k == 0 else device,
+                                       seed=inputs.BASE_SEED + k)
+            if vp.p_logits.device != torch.device(device):
+                vp = inputs.VerifyProblem(*(t.to(device) for t in (vp.p_logits, vp.q_logits, vp.u_accept,
+                                                                   vp.u_resample, vp.u_draft)))
+            ur = vp.u_resample
+            if resample == "inverse_cdf":  # one uniform per sequence
+                ur = inputs.uniform_accept((batch,), f"verify.u1.B{batch}.{k}", device=device)
+            # drafts: the linear sampler's drafting half, a single token drawn from q
+            # (at the verifier's temperature) at each position
+            qd = vp.q_logits if temperature == 1.0 else (vp.q_logits.double() / temperature).float()
+            draft, dst = binding.uno_draft_sample(qd, vp.u_draft)
+            del qd
+            assert int(dst.abs().sum()) == 0
+            vout = tuple(torch.empty(sh, dtype=torch.int32, device=device)
+                         for sh in [(batch,), (batch, BLOCK + 1), (batch,), (batch,)])
+            self.vsets.append({"p": vp.p_logits, "q": vp.q_logits, "ua": vp.u_accept, "ur": ur,
+                               "draft": draft, "vout": vout})
+            del vp
+        s0 = self.vsets[0]
+        self.p, self.q, self.ua, self.ur, self.draft, self.vout = (s0[k] for k in
+                                                                   ("p", "q", "ua", "ur", "draft", "vout"))
         self.vws = torch.empty(binding.uno_verify_block_workspace(batch, BLOCK, BLOCK, VOCAB),
                                dtype=torch.uint8, device=device)
         # kernels of this library per step: per group a one-CTA flag reset and the
@@ -296,15 +321,27 @@ class Step:
         for probs, ws in self.groups:
             binding.uno_gated_lora_linear_batched(probs, workspace=ws)
 
-    def verify(self):
+    def verify(self, k=0):
+        """The verifier on input set k."""
         from lossless_draft_verify_gated_b300 import binding
+        v = self.vsets[k]
         if self.plain:
-            binding.uno_verify_block(self.p, self.q, self.draft, self.ua, self.ur, out=self.vout,
+            binding.uno_verify_block(v["p"], v["q"], v["draft"], v["ua"], v["ur"], out=v["vout"],
                                      workspace=self.vws)
         else:
-            binding.uno_verify_block_ex(self.p, self.q, self.draft, self.ua, self.ur,
+            binding.uno_verify_block_ex(v["p"], v["q"], v["draft"], v["ua"], v["ur"],
                                         temperature=self.temperature, resample=self.resample,
-                                        out=self.vout, workspace=self.vws)
+                                        out=v["vout"], workspace=self.vws)
+
+    def set_of_step(self, i):
+        return i % len(self.vsets)
+
+    def verify_results(self, steps):
+        """Host copies of every set's outputs and the tokens verified over
+        `steps` steps (step i verified set i mod the number of sets)."""
+        res = [tuple(t.cpu() for t in v["vout"]) for v in self.vsets]
+        tokens = sum(int(res[self.set_of_step(i)][2].sum()) for i in range(steps))
+        return res, tokens
 
 
 class Timer:
@@ -312,10 +349,12 @@ class Timer:
     and times each half with CUDA events on the launching stream, with an L2
     flush (a write of twice the L2 size) before every step outside the events."""
 
-    def __init__(self, st, dev, graph=True):
+    def __init__(self, st, dev, graph=True, l2_flush="write_read"):
         import torch
         self.st = st
-        self.flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        self.flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        self.flush_read = (torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+                           if l2_flush == "write_read" else None)
         self.g_proj = self.g_ver = None
         if graph:
             s = torch.cuda.Stream(device=dev)
@@ -326,12 +365,15 @@ class Timer:
             torch.cuda.current_stream().wait_stream(s)
             torch.cuda.synchronize()
             self.g_proj = torch.cuda.CUDAGraph() if st.groups else None
-            self.g_ver = torch.cuda.CUDAGraph()
             if self.g_proj is not None:
                 with torch.cuda.graph(self.g_proj):
                     st.projections()
-            with torch.cuda.graph(self.g_ver):
-                st.verify()
+            self.g_ver = []
+            for k in range(len(st.vsets)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    st.verify(k)
+                self.g_ver.append(g)
 
     def proj(self):
         if self.g_proj is not None:
@@ -339,15 +381,23 @@ class Timer:
         elif self.st.groups:
             self.st.projections()
 
-    def ver(self):
-        self.g_ver.replay() if self.g_ver is not None else self.st.verify()
+    def ver(self, i=0):
+        k = self.st.set_of_step(i)
+        self.g_ver[k].replay() if self.g_ver is not None else self.st.verify(k)
+
+    def flush(self):
+        """Evicts the step's inputs from L2: a write of twice its size, then
+        (write_read) a read of another such buffer, leaving clean lines."""
+        self.flush_buf.zero_()
+        if self.flush_read is not None:
+            self.flush_read.max()
 
     def warm(self, n):
         import torch
-        for _ in range(n):
-            self.flush.zero_()
+        for i in range(n):
+            self.flush()
             self.proj()
-            self.ver()
+            self.ver(i)
         torch.cuda.synchronize()
 
     def run(self, steps, barrier=None):
@@ -359,11 +409,11 @@ class Timer:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(steps):
-            self.flush.zero_()  # L2 flush, outside the timed events
+            self.flush()  # L2 flush, outside the timed events
             ev[i][0].record()
             self.proj()
             ev[i][1].record()
-            self.ver()
+            self.ver(i)
             ev[i][2].record()
         torch.cuda.synchronize()
         if barrier:
@@ -398,18 +448,19 @@ def sweep(args, dev, hbm, tflops, tflops_sustained):
     out = {"steps_per_point": args.sweep_steps, "warmup_per_point": 3, "step": [], "verifier_sigma": []}
     for b in SWEEP_BATCHES:
         st = Step(b, SIGMA, dev, args.grouping)
-        tm = Timer(st, dev)
+        tm = Timer(st, dev, l2_flush=args.l2_flush)
         tm.warm(3)
         t_step, t_proj, t_ver, _ = tm.run(args.sweep_steps)
         check_device_error()
-        n_acc, _, n_em, vstat = (t.cpu() for t in st.vout)
-        assert int(vstat.abs().sum()) == 0
+        res, tokens = st.verify_results(args.sweep_steps)
+        assert all(int(r[3].abs().sum()) == 0 for r in res)
         ms_step, ms_proj, ms_ver = (statistics.mean(t) for t in (t_step, t_proj, t_ver))
         bound, ach, peak, unit, _, _ = proj_roofline(st.M, st.n_gate1, ms_proj, hbm, tflops)
-        vb = verify_bytes(b, int((n_acc < BLOCK).sum()))
+        vb = verify_bytes(b, statistics.mean(int((r[0] < BLOCK).sum()) for r in res))
+        per_step = tokens / args.sweep_steps
         e = {"batch": b, "rows_per_projection": st.M, "ms_per_step": round(ms_step, 5),
-             "tokens_per_s": round(int(n_em.sum()) / (ms_step / 1e3), 1),
-             "verified_tokens_per_step": int(n_em.sum()),
+             "tokens_per_s": round(per_step / (ms_step / 1e3), 1),
+             "verified_tokens_per_step": round(per_step, 3), "verifier_input_sets": len(st.vsets),
              "projections": {"ms": round(ms_proj, 5), "bound": bound, "achieved": round(ach, 2),
                              "unit": unit, "frac": round(ach / peak, 4)},
              "verifier": {"ms": round(ms_ver, 5), "bytes": vb,
@@ -419,10 +470,12 @@ def sweep(args, dev, hbm, tflops, tflops_sustained):
         out["step"].append(e)
         del tm, st
         torch.cuda.empty_cache()
+    out["lm_head"] = lm_head_sweep(args, dev, hbm, tflops)
+    out["tree"] = tree_sweep(args, dev, hbm)
     for sg in SWEEP_SIGMAS:
         b = SWEEP_VERIFY_BATCH
         st = Step(b, sg, dev, with_layer=False)
-        tm = Timer(st, dev)
+        tm = Timer(st, dev, l2_flush=args.l2_flush)
         tm.warm(3)
         _, _, t_ver, _ = tm.run(args.sweep_steps)
         n_acc, _, n_em, vstat = (t.cpu() for t in st.vout)
@@ -440,6 +493,137 @@ def sweep(args, dev, hbm, tflops, tflops_sustained):
     return out
 
 
+def make_flusher(dev, mode):
+    """The L2 flush of --l2-flush as a callable (write, then optionally read)."""
+    import torch
+    wbuf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    rbuf = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if mode == "write_read" else None
+
+    def flush():
+        wbuf.zero_()
+        if rbuf is not None:
+            rbuf.max()
+    return flush
+
+
+def time_graph(fn, steps, flush):
+    """Median device time (ms) of fn replayed from a CUDA graph, L2 flushed
+    (flush()) before each replay outside the timed events."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    ts = []
+    for _ in range(3 + steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts[3:])
+
+
+def lm_head_sweep(args, dev, hbm, tflops):
+    """The LM head feeding the verifier (Llama-3-8B head [128256, 4096], block
+    16, synthetic hidden states) in each of its three strategies: the logits
+    stored and verified, the verifier's statistics taken in the GEMM's
+    epilogue with the logits stored, and with only the resampled rows
+    recomputed (no logit written).  logit_bytes = the logit traffic the
+    strategy implies (written and read back)."""
+    import torch
+    from lossless_draft_verify_gated_b300 import binding, inputs
+    flush = make_flusher(dev, args.l2_flush)
+    res = []
+    for b in SWEEP_LM_BATCHES:
+        pr = inputs.lm_head_problem(b, BLOCK, VOCAB, LM_D, device=dev)
+        W = pr.W
+        qlog = torch.matmul(pr.h[b * BLOCK:].float(), W.float().T).reshape(b, BLOCK, VOCAB)
+        draft, st = binding.uno_draft_sample(qlog, pr.u_draft)
+        del qlog
+        rows = 2 * BLOCK * b
+        flops = 2.0 * rows * LM_D * VOCAB
+        outs = {}
+        for mode in ("plain", "stats_store", "stats_recompute"):
+            ws = torch.empty(binding.uno_lm_head_verify_workspace(b, BLOCK, BLOCK, VOCAB, LM_D, mode),
+                             dtype=torch.uint8, device=dev)
+            out = tuple(torch.empty(sh, dtype=torch.int32, device=dev)
+                        for sh in [(b,), (b, BLOCK + 1), (b,), (b,)])
+            ms = time_graph(lambda: binding.uno_lm_head_verify(pr.h, W, draft, pr.u_accept, pr.u_resample,
+                                                                mode=mode, out=out, workspace=ws),
+                            args.sweep_steps, flush)
+            check_device_error()
+            outs[mode] = out
+            logit = {"plain": 8 * rows * VOCAB, "stats_store": 4 * rows * VOCAB + 8 * 2 * b * VOCAB,
+                     "stats_recompute": 8 * 2 * b * VOCAB}[mode]
+            res.append({"batch": b, "mode": mode, "ms": round(ms, 4),
+                        "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                        "frac_of_bf16_peak": round(flops / (ms / 1e3) / 1e12 / tflops, 4),
+                        "logit_bytes": logit,
+                        "tokens_per_s": round(int(out[2].sum()) / (ms / 1e3), 1)})
+            del ws
+        same = all(all(torch.equal(x, y) for x, y in zip(outs["plain"], outs[m])) for m in outs)
+        for e in res[-3:]:
+            e["same_outputs_as_plain"] = same
+        del pr, W, draft, outs
+        torch.cuda.empty_cache()
+    return res
+
+
+def tree_sweep(args, dev, hbm):
+    """The tree sampler's verification on top-k trees (children of each node =
+    its most likely tokens, so acceptance is realistic) at vocab 128256: node
+    rows read once (4 bytes per logit) plus one race row."""
+    import torch
+    from lossless_draft_verify_gated_b300 import binding, inputs
+    flush = make_flusher(dev, args.l2_flush)
+    res = []
+    for b, widths in SWEEP_TREE:
+        n1 = 1
+        level = 1
+        for w in widths:
+            level *= w
+            n1 += level
+        lg = inputs.normal((b, n1, VOCAB), 8.0, f"tree.lg.B{b}.N{n1}", device=dev)
+        par = torch.full((b, n1), -1, dtype=torch.int32, device=dev)
+        tok = torch.zeros((b, n1), dtype=torch.int32, device=dev)
+        # top-k children, breadth first (the drafting half of the tree sampler)
+        nxt, frontier = 1, [0]
+        for w in widths:
+            new = []
+            for node in frontier:
+                top = torch.topk(lg[:, node], w, dim=-1).indices.to(torch.int32)
+                for k in range(w):
+                    par[:, nxt] = node
+                    tok[:, nxt] = top[:, k]
+                    new.append(nxt)
+                    nxt += 1
+            frontier = new
+        ua = inputs.uniform_accept((b, n1), f"tree.ua.B{b}", device=dev)
+        ur = inputs.uniform_race((b, VOCAB), f"tree.ur.B{b}", device=dev)
+        ws = torch.empty(binding.uno_tree_verify_workspace(b, n1 - 1, VOCAB), dtype=torch.uint8, device=dev)
+        out = (torch.empty(b, dtype=torch.int32, device=dev), torch.empty((b, n1 - 1), dtype=torch.int32, device=dev),
+               torch.empty((b, n1), dtype=torch.int32, device=dev), torch.empty(b, dtype=torch.int32, device=dev),
+               torch.empty(b, dtype=torch.int32, device=dev))
+        ms = time_graph(lambda: binding.uno_tree_verify(lg, par, tok, ua, ur, out=out, workspace=ws),
+                        args.sweep_steps, flush)
+        by = 4 * b * n1 * VOCAB + 8 * b * VOCAB
+        res.append({"batch": b, "nodes": n1, "widths": list(widths), "ms": round(ms, 5),
+                    "mean_accepted_depth": round(float(out[0].float().mean()), 3),
+                    "tokens_per_s": round(int(out[3].sum()) / (ms / 1e3), 1),
+                    "bytes": by, "frac_hbm": round(by / (ms / 1e3) / 1e9 / hbm, 4)})
+        del lg, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_uno(args):
     import torch
     ws, rank, local = dist_setup(args.gpus)
@@ -455,30 +639,32 @@ def run_uno(args):
               host_inputs=check_parity)
     K = args.steps
     with Clocks(local) as clk:
-        tm = Timer(st, dev, graph=not args.no_graph)
+        tm = Timer(st, dev, graph=not args.no_graph, l2_flush=args.l2_flush)
         tm.warm(args.warmup)
         check_device_error()
         barrier = torch.distributed.barrier if ws > 1 else None
         t_step, t_proj, t_ver, wall = tm.run(K, barrier)
     device_error = check_device_error()
-    n_acc, toks, n_em, vstat = (t.cpu() for t in st.vout)
-    assert int(vstat.abs().sum()) == 0
-    ms_step, tokens_all = aggregate(sum(t_step) / K, int(n_em.sum()), ws, dev)
-    tokens = tokens_all // ws  # per replica (every replica runs the same seeded step)
+    res, tokens_run = st.verify_results(K)
+    assert all(int(r[3].abs().sum()) == 0 for r in res)
+    # tokens per step of this replica, summed over the replicas
+    ms_step, tokens_all = aggregate(sum(t_step) / K, tokens_run / K, ws, dev)
+    tokens = tokens_all / ws  # per replica (every replica runs the same seeded steps)
     value = tokens_all / (ms_step / 1e3)
 
     # roofline of the dominant op: the layer's gated-LoRA projections
     ms_proj = statistics.mean(t_proj)
     ms_ver = statistics.mean(t_ver)
     bound, achieved, peak, unit, by, fl = proj_roofline(st.M, st.n_gate1, ms_proj, hbm, tflops)
-    n_race = int((n_acc < BLOCK).sum())
+    n_race = statistics.mean(int((r[0] < BLOCK).sum()) for r in res)
     vb = verify_bytes(args.batch, n_race, args.resample)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(args, args.batch, ws),
-        "verified_tokens_per_step": tokens,
+        "verified_tokens_per_step": round(tokens, 3),
+        "verifier_input_sets": len(st.vsets),
         "launch": "CUDA graph per half-step" if tm.g_ver is not None else "eager",
         "inputs": "CPU-drawn seeded inputs copied to the device" if check_parity else
                   "seeded inputs drawn on the device",
@@ -745,8 +931,48 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile(args):
+    """A few replays of one op for ncu: its launches are those of the sweep's
+    figure for the same batch (and, for the LM head, strategy)."""
+    import torch
+    from lossless_draft_verify_gated_b300 import binding, inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    b = args.batch
+    if args.profile == "lm_head":
+        pr = inputs.lm_head_problem(b, BLOCK, VOCAB, LM_D, device=dev)
+        draft = torch.randint(0, VOCAB, (b, BLOCK), dtype=torch.int32, device=dev,
+                              generator=inputs.generator("profile.draft", device=dev))
+        ws = torch.empty(binding.uno_lm_head_verify_workspace(b, BLOCK, BLOCK, VOCAB, LM_D, args.lm_mode),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: binding.uno_lm_head_verify(pr.h, pr.W, draft, pr.u_accept, pr.u_resample,  # noqa: E731
+                                                mode=args.lm_mode, workspace=ws)
+    else:
+        widths, n1, level = (3, 2, 2, 1), 1, 1
+        for w in widths:
+            level *= w
+            n1 += level
+        lg = inputs.normal((b, n1, VOCAB), 8.0, f"tree.lg.B{b}.N{n1}", device=dev)
+        par = torch.full((b, n1), -1, dtype=torch.int32, device=dev)
+        tok = torch.zeros((b, n1), dtype=torch.int32, device=dev)
+        par[:, 1:] = 0  # a star of n1-1 children at the root: the widest walk
+        tok[:, 1:] = torch.topk(lg[:, 0], n1 - 1, dim=-1).indices.to(torch.int32)
+        ua = inputs.uniform_accept((b, n1), f"tree.ua.B{b}", device=dev)
+        ur = inputs.uniform_race((b, VOCAB), f"tree.ur.B{b}", device=dev)
+        fn = lambda: binding.uno_tree_verify(lg, par, tok, ua, ur)  # noqa: E731
+    flush = make_flusher(dev, args.l2_flush)
+    for _ in range(args.warmup + args.steps):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    check_device_error()
+
+
 def main():
     args = parse()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

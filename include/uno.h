@@ -374,8 +374,6 @@ int uno_draft_sample(const float *logits, const float *u, int64_t R, int64_t V,
 /* Device error word of this library on the current device (synchronous).
  * Bit 0 is set when a pipeline wait inside a projection kernel exceeded its
  * 2-second limit; that kernel unwound without writing its output tile.
- * Bit 1 is set when a wait of the one-launch verifier (small batches) ran out;
- * that call's outputs are invalid.
  * reset != 0 clears the word.  Returns the word (>= 0) or UNO_ERR_CUDA. */
 int uno_device_error(int reset);
 

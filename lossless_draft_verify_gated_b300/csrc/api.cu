@@ -274,12 +274,6 @@ int uno_draft_sample(const float* logits, const float* u, int64_t R, int64_t V, 
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
 
-int uno_device_error(int reset) {
-  const int g = read_device_error(reset);
-  if (g < 0) return g;
-  const int v = read_verify_error(reset);
-  if (v < 0) return v;
-  return g | (v << 1);
-}
+int uno_device_error(int reset) { return read_device_error(reset); }
 
 }  // extern "C"

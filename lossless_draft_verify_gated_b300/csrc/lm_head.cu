@@ -11,7 +11,7 @@
 // sequence that is resampled.  Three strategies, the same result:
 //
 //   PLAIN       the head GEMM stores fp32 logits, the verifier of verify.cu
-//               (or verify_fused.cu) reads them;
+//               reads them;
 //   STATS_STORE the GEMM's epilogue leaves the statistics (per row and
 //               vocabulary tile) and also stores the logits; a decide kernel
 //               takes the accept decisions from the statistics and a race

@@ -23,9 +23,9 @@ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) & ~(a - 1); }
 // Kp in {K, K+1} with Kp >= 1, 1 <= V < 2^31, 0 <= Bn <= 2^24.
 bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V);
 
-// Largest batch the one-launch verifier (verify_fused.cu) takes: at batch 1 it
-// matches the two launches (about 29 us on a B300), above it they are faster.
-constexpr int64_t kFusedMaxBatch = 1;
+// Sequences from which the verifier's finish kernel is launched as a
+// programmatic dependent of its statistics kernel.
+constexpr int64_t kFinishPdlMinBatch = 8;
 
 struct VerifyPlan {
   int64_t rows;      // Bn * (Kp + K): AR rows then draft rows of each sequence
@@ -33,21 +33,9 @@ struct VerifyPlan {
   int64_t chunk;     // elements per chunk (multiple of 4)
   int race_splits;   // vocab chunks per sequence in the resampling race
   int64_t race_chunk;
-  size_t off_stats, off_gather, off_race, off_count;
-  // one-launch path (small batches): CTAs, row segments and race rows per CTA
-  bool fused;
-  int fused_G, fused_Gs, fused_S;  // CTAs, CTAs with a statistics slice, slots per row
-  size_t off_fpart, off_fgather, off_frace, off_fsync, fused_bytes;
-  size_t bytes;      // workspace for either path
+  size_t off_stats, off_gather, off_race, off_count, bytes;
 };
 VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms);
-void plan_verify_fused(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms, VerifyPlan& pl);
-cudaError_t launch_verify_fused(const float* p, const float* q, const int32_t* draft,
-                                const float* u_acc, const float* u_res, int64_t Bn, int64_t K,
-                                int64_t Kp, int64_t V, int32_t* n_acc, int32_t* out_tokens,
-                                int32_t* n_emit, int32_t* status, void* ws, const VerifyPlan& pl,
-                                cudaStream_t st);
-int read_verify_error(int reset);
 
 cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                           const float* u_acc, const float* u_res, int64_t Bn,

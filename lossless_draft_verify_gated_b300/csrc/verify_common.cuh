@@ -1,7 +1,7 @@
 // verify_common.cuh -- device helpers shared by the verifier kernels
-// (verify.cu: the two-launch verifier and draft sampler; verify_fused.cu: the
-// one-launch verifier for small batches): the online (max, sum exp) of a
-// logit row and the candidates of the exponential race.
+// (verify.cu: the block verifier and draft sampler; tree.cu: the tree
+// sampler; lm_head.cu: the LM head's decide and race kernels): the online
+// (max, sum exp) of a logit row and the candidates of the exponential race.
 #pragma once
 
 #include <cmath>

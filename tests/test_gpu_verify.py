@@ -69,7 +69,8 @@ def test_verify_parity_step_sweep(Bn):
 
 def _shifted(t):
     """A contiguous copy of t whose data start 4 bytes past a 16-byte boundary
-    (rows stay 4-byte aligned): the verifier then takes its two-launch path."""
+    (rows stay 4-byte aligned): the statistics pass then reads every row
+    through its scalar head and tail."""
     buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)
     v = buf[1:1 + t.numel()].view(t.shape)
     v.copy_(t)
@@ -79,10 +80,11 @@ def _shifted(t):
 
 @pytest.mark.parametrize("Bn,K,V,Kp", [(1, 16, 128256, None), (3, 16, 128256, 17),
                                        (16, 16, 128256, None), (5, 7, 1000, 8), (16, 4, 64, None)])
-def test_one_launch_and_two_launch_paths(Bn, K, V, Kp):
-    """Small batches with a vocabulary divisible by 4 and 16-byte aligned rows
-    take the one-launch verifier; the same inputs 4 bytes off alignment take
-    the two-launch kernels.  Both match the oracle."""
+def test_aligned_and_unaligned_rows(Bn, K, V, Kp):
+    """The same inputs from 16-byte aligned rows and from rows 4 bytes off
+    alignment (the vectorised statistics pass's head/tail path) match the
+    oracle and each other, at batches on both sides of the finish kernel's
+    programmatic-launch threshold."""
     from lossless_draft_verify_gated_b300 import uno_device_error, uno_verify_block
     pr = inputs.verify_problem(Bn, K, V, Kp=Kp, sigma=1.0, seed=77)
     draft, st, _ = oracle.draft_sample(pr.q_logits, pr.u_draft)
