@@ -319,7 +319,7 @@ cudaError_t launch_tree_verify(const float* logits, const int32_t* parent, const
   cfg.blockDim = dim3(kTT);
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = Bn >= kFinishPdlMinBatch ? 1 : 0;  // (see launch_verify)
+  cfg.numAttrs = 1;  // (see launch_verify)
   return cudaLaunchKernelEx(&cfg, tree_finish_kernel, logits, parent, token, u_acc, u_res, N, V,
                             pl.splits, pl.race_splits, pl.race_chunk,
                             reinterpret_cast<const float2*>(w + pl.off_stats),

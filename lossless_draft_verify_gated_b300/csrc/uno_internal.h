@@ -23,10 +23,6 @@ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) & ~(a - 1); }
 // Kp in {K, K+1} with Kp >= 1, 1 <= V < 2^31, 0 <= Bn <= 2^24.
 bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V);
 
-// Sequences from which the verifier's finish kernel is launched as a
-// programmatic dependent of its statistics kernel.
-constexpr int64_t kFinishPdlMinBatch = 8;
-
 struct VerifyPlan {
   int64_t rows;      // Bn * (Kp + K): AR rows then draft rows of each sequence
   int splits;        // vocab chunks per row in the statistics pass

@@ -48,6 +48,8 @@ __device__ __forceinline__ void grid_launch_dependents() {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;  // float4 loads in flight per thread in the statistics pass
+constexpr int kStatsCtasPerSm = 8;  // statistics CTAs resident on an SM at once
+constexpr int kFinishCtasPerSm = 4;  // finish CTAs resident on an SM at once
 constexpr int kRace = 0, kInverseCdf = 1;  // resample modes (uno.h: UNO_RESAMPLE_*)
 
 // Row j of sequence b: j < Kp is AR row j, else draft row j - Kp.
@@ -57,8 +59,10 @@ __device__ __forceinline__ const float* row_ptr(const float* p, const float* q, 
 }
 
 // kEx: logits at a temperature other than 1 (the plain kernel is kept as it was)
+// At most 32 registers a thread, so that 8 CTAs fit on an SM and the grid the
+// plan sizes for small batches runs as a single wave.
 template <bool kEx>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kStatsCtasPerSm)
 verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
                     const int32_t* __restrict__ draft, int64_t K, int64_t Kp, int64_t V,
                     int splits, int64_t chunk, float inv_t, float2* __restrict__ part,
@@ -69,43 +73,37 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const int64_t per_seq = Kp + K;
   const int64_t b = row / per_seq;
   const int64_t j = row - b * per_seq;
-  // The finish kernel may start once every earlier launch has finished; it
-  // waits for this one before it reads what this one writes.
   grid_dependency_wait();
-  if (threadIdx.x == 0) grid_launch_dependents();
   if (j == 0 && split == 0 && threadIdx.x == 0) counter[b] = 0;  // finish kernel's arrival count
-  // The drafted token of this row's position (AR row j or draft row j - Kp);
-  // the thread that streams its logit keeps it for the acceptance test.
-  const int64_t pos = j < Kp ? j : j - Kp;
-  const int64_t xd = pos < K ? int64_t(draft[b * K + pos]) : -1;
-
-  const float* r = row_ptr(p, q, b, j, K, Kp, V);
+  // This CTA's chunk [v0, v0 + n) of the row, addressed from its start with
+  // 32-bit offsets (a chunk holds < 2^31 elements).
   const int64_t v0 = int64_t(split) * chunk;
-  const int64_t v1 = min(V, v0 + chunk);
-  // 16-byte aligned body [va, vb), scalar head [v0, va) and tail [vb, v1).
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(r + v0);
-  const int64_t head_raw = int64_t(((16 - (addr & 15)) & 15) >> 2);
-  const int64_t head = head_raw < v1 - v0 ? head_raw : v1 - v0;
-  const int64_t va = v0 + head;
-  const int64_t nvec = (v1 - va) >> 2;
-  const int64_t vb = va + nvec * 4;
+  const float* r = row_ptr(p, q, b, j, K, Kp, V) + v0;
+  const int n = int(min(V - v0, chunk));
+  // The drafted token of this row's position (AR row j or draft row j - Kp):
+  // the CTA whose chunk holds it stores its logit for the acceptance test.
+  const int64_t pos = j < Kp ? j : j - Kp;
+  if (pos < K && threadIdx.x == 0) {
+    const int64_t xd = int64_t(draft[b * K + pos]) - v0;
+    if (xd >= 0 && xd < n) gathered[row] = r[xd];
+  }
+  // 16-byte aligned body [head, head + 4 * nv), scalar head and tail.
+  const int head_raw = int(((16 - (reinterpret_cast<uintptr_t>(r) & 15)) & 15) >> 2);
+  const int head = head_raw < n ? head_raw : n;
+  const int nv = (n - head) >> 2;
+  const int tail = head + nv * 4;
 
   MS acc{-INFINITY, 0.f};
   const int tid = threadIdx.x;
-  if (tid < va - v0) {
-    const float x = r[v0 + tid];
+  if (tid < head) {
+    const float x = r[tid];
     ms_add1(acc, kEx ? x * inv_t : x);
-    if (v0 + tid == xd) gathered[row] = x;
   }
-  if (tid < v1 - vb) {
-    const float x = r[vb + tid];
+  if (tail + tid < n) {
+    const float x = r[tail + tid];
     ms_add1(acc, kEx ? x * inv_t : x);
-    if (vb + tid == xd) gathered[row] = x;
   }
-  const float4* vp = reinterpret_cast<const float4*>(r + va);
-  // chunks hold < 2^31 elements: 32-bit indices in the streaming loop
-  const int nv = int(nvec);
-  const int xq = (xd >= va && xd < vb) ? int((xd - va) >> 2) : -1;  // float4 holding the drafted token
+  const float4* vp = reinterpret_cast<const float4*>(r + head);
   for (int i = tid; i < nv; i += kThreads * kUnroll) {
     float4 t[kUnroll];
 #pragma unroll
@@ -119,10 +117,6 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
         ms_add4(acc, t[u].x * inv_t, t[u].y * inv_t, t[u].z * inv_t, t[u].w * inv_t);
       else
         ms_add4(acc, t[u].x, t[u].y, t[u].z, t[u].w);
-      if (xq == i + u * kThreads) {
-        const int c = int((xd - va) & 3);
-        gathered[row] = c == 0 ? t[u].x : c == 1 ? t[u].y : c == 2 ? t[u].z : t[u].w;
-      }
     }
   }
 
@@ -134,14 +128,26 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
     MS t = red[0];
     for (int w = 1; w < kWarps; ++w) t = ms_merge(t, red[w]);
     part[unit] = make_float2(t.m, t.s);
+    // The finish kernel's CTAs may now be scheduled (they wait for this grid
+    // to complete before reading what it wrote).  Signalled at the end, not
+    // the start, so that they do not take SM slots this grid's wave needs.
+    grid_launch_dependents();
   }
 }
 
 constexpr int kMaxRows = 2 * 256 + 1;  // Kp + K rows of one sequence held in smem
 
+// Arrival count of a last-arriver merge: the add releases this CTA's earlier
+// stores and acquires those of every CTA that arrived before it.
+__device__ __forceinline__ int arrive_acq_rel(int* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
 // kEx: temperature other than 1 or the inverse-CDF resample
 template <bool kEx>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kFinishCtasPerSm)
 verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
                      const int32_t* __restrict__ draft, const float* __restrict__ u_acc,
                      const float* __restrict__ u_res, int64_t K, int64_t Kp, int64_t V,
@@ -181,44 +187,43 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   }
   if (tid == 0) s_bad = 0;
   grid_dependency_wait();  // the statistics pass's partials, gathered logits and counters
+  // the drafted tokens' logits (position tid), in flight during step 1
+  const float g_q = has_i ? gathered[b * per_seq + Kp + tid] : 0.f;
+  const float g_p = has_i ? gathered[b * per_seq + tid] : 0.f;
   __syncthreads();
 
-  // 1. Row normalisers of this sequence from the statistics partials: one
-  //    warp per row, lanes over the chunk partials, loads of four rows in
-  //    flight at once.
+  // 1. Row normalisers of this sequence from the statistics partials: eight
+  //    threads per row (32 rows at a time), each merging every eighth chunk
+  //    partial, then three shuffle rounds inside the group of eight.
   {
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int64_t j0 = int64_t(warp) * 4; j0 < per_seq; j0 += kWarps * 4) {
-      MS t[4];
+    const int sub = tid & 7;
+    for (int64_t j0 = 0; j0 < per_seq; j0 += kThreads / 8) {
+      const int64_t j = j0 + (tid >> 3);
+      MS t{-INFINITY, 0.f};
+      if (j < per_seq) {
+        const float2* pj = part + (b * per_seq + j) * splits;
+        for (int s0 = sub; s0 < splits; s0 += 32) {
+          float2 v[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) t[r] = MS{-INFINITY, 0.f};
-      for (int s0 = 0; s0 < splits; s0 += 64) {
-        float2 v[4][2];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int s = s0 + lane + 32 * h;
-            const int64_t j = j0 + r;
-            v[r][h] = (j < per_seq && s < splits) ? part[(b * per_seq + j) * splits + s]
-                                                  : make_float2(-INFINITY, 0.f);
+          for (int u = 0; u < 4; ++u) {
+            const int sx = s0 + 8 * u;
+            v[u] = sx < splits ? pj[sx] : make_float2(-INFINITY, 0.f);
           }
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) t[r] = ms_merge(t[r], MS{v[r][h].x, v[r][h].y});
+          for (int u = 0; u < 4; ++u) t = ms_merge(t, MS{v[u].x, v[u].y});
+        }
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const MS m = warp_merge(t[r]);
-        const int64_t j = j0 + r;
-        if (lane == 0 && j < per_seq) {
-          const bool bad = isnan(m.s) || !(m.m > -INFINITY) || !(m.m < INFINITY) || !(m.s > 0.f);
-          if (bad) atomicOr(&s_bad, 2);
-          s_m[j] = m.m;
-          s_lz[j] = m.m + logf(m.s);
-          s_iz[j] = 1.0f / m.s;
-        }
+      for (int o = 4; o > 0; o >>= 1) {
+        const MS u{__shfl_xor_sync(0xffffffffu, t.m, o), __shfl_xor_sync(0xffffffffu, t.s, o)};
+        t = ms_merge(t, u);
+      }
+      if (sub == 0 && j < per_seq) {
+        const bool bad = isnan(t.s) || !(t.m > -INFINITY) || !(t.m < INFINITY) || !(t.s > 0.f);
+        if (bad) atomicOr(&s_bad, 2);
+        s_m[j] = t.m;
+        s_lz[j] = t.m + logf(t.s);
+        s_iz[j] = 1.0f / t.s;
       }
     }
   }
@@ -245,12 +250,12 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   if (has_i) {
     const int i = tid;
     // logits of the drafted token, gathered by the statistics pass
-    const float lq = gathered[b * per_seq + Kp + i];
+    const float lq = g_q;
     bool accept;
     if (lq == -INFINITY) {
       accept = true;  // q_i(x) = 0: ratio +inf
     } else {
-      const float lp = gathered[b * per_seq + i];
+      const float lp = g_p;
       const float lr = kEx ? (lp * inv_t - s_lz[i]) - (lq * inv_t - s_lz[Kp + i])
                            : (lp - s_lz[i]) - (lq - s_lz[Kp + i]);
       const float thr = fminf(1.0f, expf(lr));
@@ -331,12 +336,12 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
         c += s_d[1][w];
       }
       csum[split] = make_longlong2(a, c);
-      __threadfence();
-      s_last = atomicAdd(&counter[b], 1) == race_splits - 1;
+      s_last = arrive_acq_rel(&counter[b]) == race_splits - 1;
     }
+    // thread 0's acquire, then the barrier, order the loads below after
+    // every other CTA's chunk sums
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     // (a) the chunk holding the crossing
     const int per = (race_splits + kThreads - 1) / kThreads;
     const int c_lo = min(race_splits, tid * per), c_hi = min(race_splits, c_lo + per);
@@ -485,8 +490,7 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
     int last = 1;
     if (race_splits > 1) {
       rpart[b * race_splits + split] = RacePart{cr.s, cr.v, cp.s, cp.v};
-      __threadfence();
-      last = atomicAdd(&counter[b], 1) == race_splits - 1;
+      last = arrive_acq_rel(&counter[b]) == race_splits - 1;
     }
     s_last = last;
   }
@@ -494,8 +498,8 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
   if (!s_last) return;
   if (race_splits > 1) {
     // The last CTA of the sequence merges every chunk's winner (loads spread
-    // over the block, then the same warp/block reduction).
-    __threadfence();
+    // over the block, then the same warp/block reduction); thread 0's
+    // acquire and the barrier above order them after every chunk's store.
     cr = Cand{0.f, -1};
     cp = Cand{-1.f, -1};
     for (int s = tid; s < race_splits; s += kThreads) {
@@ -574,19 +578,19 @@ draft_sample_kernel(const float* __restrict__ logits, const float* __restrict__ 
 VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   VerifyPlan pl{};
   pl.rows = Bn * (Kp + K);
-  // Statistics pass: about 8 CTAs of 256 threads per SM; split rows only
-  // while each chunk keeps at least 2048 logits.
-  const int64_t target = int64_t(sms) * 8;
+  // Statistics pass: one wave of kStatsCtasPerSm CTAs of 256 threads per SM;
+  // split rows only while each chunk keeps at least 2048 logits.
+  const int64_t target = int64_t(sms) * kStatsCtasPerSm;
   int64_t s = pl.rows > 0 ? (target + pl.rows - 1) / pl.rows : 1;
   s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 2047) / 2048));
   int64_t chunk = (V + s - 1) / s;
   chunk = (chunk + 3) & ~int64_t(3);
   pl.chunk = chunk;
   pl.splits = int((V + chunk - 1) / chunk);
-  // Race pass: about 4 CTAs per SM, chunks of at least 1024 entries (one
-  // batch of loads per thread at small batch).
-  const int64_t rt = int64_t(sms) * 4;
-  int64_t s2 = Bn > 0 ? (rt + Bn - 1) / Bn : 1;
+  // Race pass: at most kFinishCtasPerSm CTAs per SM (one wave), chunks of at
+  // least 1024 entries (one batch of loads per thread at small batch).
+  const int64_t rt = int64_t(sms) * kFinishCtasPerSm;
+  int64_t s2 = Bn > 0 ? rt / Bn : 1;
   s2 = std::max<int64_t>(1, std::min<int64_t>(s2, (V + 1023) / 1024));
   pl.race_chunk = (V + s2 - 1) / s2;
   pl.race_splits = int((V + pl.race_chunk - 1) / pl.race_chunk);
@@ -610,12 +614,11 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
   RacePart* rpart = reinterpret_cast<RacePart*>(w + pl.off_race);
   int* counter = reinterpret_cast<int*>(w + pl.off_count);
   const int64_t g1 = pl.rows * pl.splits;
-  // The statistics kernel is launched with programmatic stream serialization:
-  // it may start while the launch before it drains, and waits for it
+  // Both kernels are launched with programmatic stream serialization: each
+  // may start while the launch before it drains, and waits for it
   // (griddepcontrol.wait) before it reads anything that launch writes.  The
-  // finish kernel is too from kFinishPdlMinBatch sequences: below that, its
-  // CTAs made resident early take slots from the statistics pass's single
-  // wave (batch 1: 26.6 us with it against 22.5 us without on a B300).
+  // statistics CTAs signal the finish kernel only as they end, so its CTAs
+  // become resident as the statistics wave drains, not during it.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -631,7 +634,6 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                                           pl.splits, pl.chunk, inv_t, part, gathered, counter);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(unsigned(Bn * pl.race_splits));
-  cfg.numAttrs = Bn >= kFinishPdlMinBatch ? 1 : 0;
   e = ex ? cudaLaunchKernelEx(&cfg, verify_finish_kernel<true>, p, q, draft, u_acc, u_res, K, Kp, V,
                               pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
                               (const float2*)part, (const float*)gathered, rpart, counter, n_acc,
