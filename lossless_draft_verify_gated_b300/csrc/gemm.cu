@@ -10,8 +10,9 @@
 // projections (for example the seven projections of a transformer layer).
 //
 // Work is split into 64-wide K-blocks, in two sections:
-//   * the down section: tiles of T = bf16(gate * alpha/rank * x.A^T), one
-//     run of tiles per problem with a nonzero rank;
+//   * the down section (token-row order only): tiles of
+//     T = bf16(gate * alpha/rank * x.A^T), one run of tiles per problem with
+//     a nonzero rank;
 //   * the main section: tiles of y, each a flat run of rank/64 adapter
 //     K-blocks (A-operand B, B-operand T) followed by d_in/64 base K-blocks
 //     (x.W^T).  The adapter accumulates into the same TMEM accumulator as
@@ -40,8 +41,12 @@
 // accumulator (tcgen05.ld) and store y, T or partials, overlapping the next
 // piece's MMAs.
 // Decode-sized M (<= 128 token rows) swaps the operands so that the weights
-// fill the 128-row MMA side and the tokens are N; short decode launches give
-// each piece its own share of the adapter instead of shared T tiles.  Larger
+// fill the 128-row MMA side and the tokens are N, and computes T by split K
+// in the epilogue warps, which are idle until a CTA's first accumulator is
+// full: CTA c computes the partial T of one chunk of one problem's d_in with
+// warp-level MMAs, then, once every chunk of that problem is in, sums a slice
+// of T over the chunks in a fixed order and publishes it; the weight stream
+// never carries the down matrix and no T tile waits on a merge.  Larger
 // M takes tiles of 128 tokens x 256 (or 128) outputs and, with at least one
 // tile per CTA, deals whole tiles out in data-parallel waves (no splits).
 // Launches are chained with programmatic dependent launch: each CTA lets the
@@ -82,6 +87,10 @@ constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
 constexpr int kPrefetchKBlocks = 8;  // weight tiles hinted into L2 before the previous launch ends
 constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;
 constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand
+constexpr bool kSplitKAdapter = true;  // decode order: T by split K in the epilogue warps
+// (up to 64 token rows: the operands of a chunk are staged in the finisher
+// staging area, which exists for tiles of at most 64 tokens)
+constexpr int64_t kSplitKMaxRows = 64;
 constexpr int kDown = 0, kMain = 1;
 
 enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, kMapsPerProblem = 5 };
@@ -111,9 +120,10 @@ struct Prob {
   void* t;
   const uint8_t* gate;
   float scale;
+  int d_in;
   int d_out;
   int r;
-  int tflag0;  // first T-ready flag of the problem
+  int tflag0;  // first T-ready flag of the problem (split-K adapter: [chunks in, slices out])
   int ttiles;  // T tiles of the problem
   int f32out;  // store y as fp32 (bf16 operands)
   // Statistics epilogue (logit rows of the verifier, rank 0): instead of (or
@@ -137,6 +147,16 @@ struct Params {
   int nprob;           // problems of the launch
   int swap;
   int localt;  // swap path with per-piece adapter
+  // Split-K adapter (decode order): the epilogue warps of CTA c < tchunks
+  // compute the partial T of chunk c (tkpc K-blocks of one problem's d_in;
+  // problem p owns chunks [tch0[p], tch0[p+1])), then reduce a slice of T.
+  int tsplit;
+  int tkpc;
+  int tchunks;
+  int tbn;  // rows of the x boxes (tokens, rounded up to the tile width)
+  int tch0[kMaxLoraProblems + 1];
+  int64_t tpart_stride;  // floats between chunk partials ([M][r] each)
+  float* tpart;
   int M;
   int out_f32;
   int grid;
@@ -204,8 +224,10 @@ __host__ __device__ constexpr uint32_t tmem_cols() {
 // Barriers and the TMEM slot, then a copy of the kernel parameters.
 constexpr uint32_t kBarrierBytes = 512;
 constexpr uint32_t kParamsBytes = (uint32_t(sizeof(Params)) + 15u) & ~15u;
-// Decode order: the gates of every problem's tokens, staged once per CTA.
-constexpr uint32_t kGateBytes = uint32_t(kMaxLoraProblems) * uint32_t(kSwapMaxRows);
+// Decode order: the gates of every problem's tokens, staged once per CTA,
+// then the split-K adapter's reduction scratch (one float4 per epilogue thread).
+constexpr uint32_t kGateOnlyBytes = uint32_t(kMaxLoraProblems) * uint32_t(kSwapMaxRows);
+constexpr uint32_t kGateBytes = kGateOnlyBytes + 2048;
 template <int BNMAX, bool LOCALT>
 __host__ __device__ constexpr uint32_t smem_bytes_for() {
   return uint32_t(stages_for<BNMAX, LOCALT>()) * stage_bytes<BNMAX, LOCALT>() +
@@ -339,6 +361,19 @@ __device__ __forceinline__ int ld_relaxed(const int* p) {
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
+__device__ __forceinline__ void red_add_relaxed(int* p, int v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Waits until the counter at f reaches target (acquire), for at most limit_ns.
+__device__ __forceinline__ bool wait_count(const int* f, int target, uint64_t limit_ns) {
+  if (ld_acquire(f) >= target) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ld_acquire(f) < target) {
+    __nanosleep(64);
+    if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
 __device__ __forceinline__ bool wait_flag(const int* f, uint64_t limit_ns) {
   if (ld_acquire(f)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -465,6 +500,197 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
   ptx::tmem_ld_wait(r);
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Split-K adapter, run by the 128 epilogue threads of CTA `cta` < tchunks
+// before their first accumulator arrives (they are idle until then):
+//   1. the partial T_c[m][j] = sum_{k in chunk c} x[m,k] A[j,k] of the CTA's
+//      chunk: TMA brings the chunk's K-blocks of A and x into the staging
+//      area (128-byte swizzle, as for the main operands) in as few rounds as
+//      it holds; warp w multiplies rank rows 32w..32w+31 of every 128 with
+//      warp-level MMAs; the partial is stored as fp32 [M][r] and counted in;
+//   2. once all nch chunks of the problem are in, slice idx of the [M][r]
+//      entries summed over the chunks -- each thread a fixed stride of
+//      chunks, then the stride groups in order, so every run adds in the same
+//      order -- and stored as T = bf16(gate[m] * alpha/r * sum), counted out.
+// A main tile's adapter K-blocks wait for every slice of their problem.
+// Counts are released by a fence and a relaxed add (one fence, not two).
+// Returns false if a wait gave up.
+__device__ bool tsplit_run(const Params& P, const Maps& maps, int cta, int et,
+                           const uint8_t* gate_s, float4* red, uint8_t* stg, uint32_t stg_bytes,
+                           uint64_t* stg_bar, uint32_t& stg_phase) {
+  const int ch = cta;
+  int p = 0;
+  while (P.tch0[p + 1] <= ch) ++p;
+  const Prob& pb = P.pb[p];
+  const int nch = P.tch0[p + 1] - P.tch0[p];
+  const int idx = ch - P.tch0[p];
+  const int r = pb.r, M = P.M;
+  const int nkb_p = (pb.d_in + kBK - 1) / kBK;
+  const int kb0 = idx * P.tkpc;
+  const int kb1 = min(nkb_p, kb0 + P.tkpc);
+  int* cnt = P.tflag + pb.tflag0;  // [0] chunks in, [1] slices out
+  {
+    const int rt = (r + kBM - 1) / kBM;                  // 128-row tiles of A
+    const uint32_t xbytes = uint32_t(P.tbn) * kBK * 2;   // one K-block of x
+    const uint32_t per_kb = uint32_t(rt) * kABytes + xbytes;
+    const int kb_round = int(stg_bytes / per_kb);        // K-blocks per round (>= 1)
+    float* part = P.tpart + int64_t(ch) * P.tpart_stride;
+    const int wq = et >> 5, lane = et & 31, g = lane >> 2, t2 = 2 * (lane & 3);
+    const CUtensorMap* mp = maps.m[p];
+    const uint32_t sbase = ptx::smem_u32(stg);
+    // 32-bit word (two bf16) at (row, k) of a 128-byte-swizzled [rows][64] tile
+    auto lds = [](uint32_t tile, int row, int k) -> uint32_t {
+      uint32_t v;
+      const uint32_t a = tile + uint32_t(row) * 128u + (uint32_t(((k >> 3) ^ row) & 7) << 4) +
+                         uint32_t(k & 7) * 2u;
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+      return v;
+    };
+    // K-blocks [kr, kr + nk) into the staging area; every thread takes part
+    // (the barrier before the copies: the area is free; the one after the
+    // wait: every thread gets the same answer)
+    auto load_round = [&](int kr, int nk) -> bool {
+      epi_sync();
+      if (et == 0) {
+        fence_proxy_async();
+        ptx::mbar_arrive_expect_tx(stg_bar, uint32_t(nk) * per_kb);
+        for (int i = 0; i < nk; ++i) {
+          uint8_t* d = stg + size_t(i) * per_kb;
+          for (int t = 0; t < rt; ++t)
+            ptx::tma_load_2d(d + size_t(t) * kABytes, &mp[MAP_A], stg_bar, (kr + i) * kBK, t * kBM,
+                             ptx::policy_evict_first());
+          ptx::tma_load_2d(d + size_t(rt) * kABytes, &mp[MAP_X], stg_bar, (kr + i) * kBK, 0,
+                           ptx::policy_evict_last());
+        }
+      }
+      const bool ok = ptx::mbar_wait(stg_bar, stg_phase & 1, kWaitLimitNs);
+      ++stg_phase;
+      return !epi_sync_or(!ok);
+    };
+    const bool once = kb1 - kb0 <= kb_round;  // the whole chunk fits: one round
+    if (once && !load_round(kb0, kb1 - kb0)) return false;
+    // passes over rank rows (128 at a time) and tokens (32 at a time), the
+    // same for every warp; a warp whose rows start beyond the rank idles
+    for (int jp = 0; jp < r; jp += kBM) {
+      for (int n0 = 0; n0 < M; n0 += 32) {
+        const int j0 = jp + wq * 32;
+        const bool active = j0 < r;
+        const int ti = jp / kBM;  // A tile of this pass
+        float acc[2][4][4];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[mi][ni][i] = 0.f;
+        for (int kr = kb0; kr < kb1; kr += kb_round) {
+          const int nk = min(kb_round, kb1 - kr);
+          if (!once && !load_round(kr, nk)) return false;
+          if (!active) continue;
+          for (int i = 0; i < nk; ++i) {
+            const uint32_t ta = sbase + uint32_t(i) * per_kb + uint32_t(ti) * kABytes;
+            const uint32_t tx = sbase + uint32_t(i) * per_kb + uint32_t(rt) * kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK; kk += 16) {
+              uint32_t a[2][4], b[4][2];
+#pragma unroll
+              for (int mi = 0; mi < 2; ++mi) {
+                const int row = wq * 32 + 16 * mi + g;  // row in the A tile (rows >= r are zero)
+                a[mi][0] = lds(ta, row, kk + t2);
+                a[mi][1] = lds(ta, row + 8, kk + t2);
+                a[mi][2] = lds(ta, row, kk + 8 + t2);
+                a[mi][3] = lds(ta, row + 8, kk + 8 + t2);
+              }
+#pragma unroll
+              for (int ni = 0; ni < 4; ++ni) {
+                const int m = n0 + 8 * ni + g;  // token rows M .. tbn-1 are the tile's zero fill
+                b[ni][0] = m < P.tbn ? lds(tx, m, kk + t2) : 0u;
+                b[ni][1] = m < P.tbn ? lds(tx, m, kk + 8 + t2) : 0u;
+              }
+#pragma unroll
+              for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) ptx::mma_bf16_16816(acc[mi][ni], a[mi], b[ni]);
+            }
+          }
+        }
+        if (!active) continue;
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int ni = 0; ni < 4; ++ni) {
+            const int j = j0 + 16 * mi + g, m = n0 + 8 * ni + t2;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int jj = j + 8 * h;
+              if (jj >= r) continue;
+              if (m < M) part[int64_t(m) * r + jj] = acc[mi][ni][2 * h];
+              if (m + 1 < M) part[int64_t(m + 1) * r + jj] = acc[mi][ni][2 * h + 1];
+            }
+          }
+      }
+    }
+  }
+  epi_sync();
+  if (et == 0) {
+    fence_acq_rel_gpu();
+    red_add_relaxed(cnt, 1);
+  }
+  bool ok = true;
+  if (et == 0) ok = wait_count(cnt, nch, kWaitLimitNs);
+  if (epi_sync_or(!ok)) return false;
+  {
+    const int64_t E4 = int64_t(M) * r / 4;  // r is a multiple of 8
+    const int64_t s0 = E4 * idx / nch, s1 = E4 * (idx + 1) / nch;
+    const float4* base = reinterpret_cast<const float4*>(P.tpart + int64_t(P.tch0[p]) * P.tpart_stride);
+    const int64_t cs4 = P.tpart_stride / 4;
+    __nv_bfloat16* T = static_cast<__nv_bfloat16*>(pb.t);  // [M][r]
+    for (int64_t e0 = s0; e0 < s1; e0 += kEpiThreads) {
+      const int S = int(s1 - e0 < kEpiThreads ? s1 - e0 : int64_t(kEpiThreads));
+      const int G2 = kEpiThreads / S;  // chunk strides
+      const int e = et % S, cg = et / S;
+      float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (cg < G2) {
+#pragma unroll 8
+        for (int c = cg; c < nch; c += G2) {
+          const float4 v = __ldcg(base + int64_t(c) * cs4 + e0 + e);
+          a4.x += v.x;
+          a4.y += v.y;
+          a4.z += v.z;
+          a4.w += v.w;
+        }
+      }
+      red[et] = a4;
+      epi_sync();
+      if (et < S) {
+        float4 sum = red[et];
+        for (int q2 = 1; q2 < G2; ++q2) {
+          const float4 v = red[q2 * S + et];
+          sum.x += v.x;
+          sum.y += v.y;
+          sum.z += v.z;
+          sum.w += v.w;
+        }
+        const int64_t ei = (e0 + et) * 4;
+        const int m = int(ei / r), j = int(ei - int64_t(m) * r);
+        const float gs = float(gate_s[p * int(kSwapMaxRows) + m]) * pb.scale;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x * gs, sum.y * gs);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z * gs, sum.w * gs);
+        *reinterpret_cast<uint2*>(T + int64_t(m) * r + j) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      }
+      epi_sync();
+    }
+  }
+  // T is read next by TMA in other CTAs
+  fence_proxy_async();
+  epi_sync();
+  if (et == 0) {
+    fence_acq_rel_gpu();
+    red_add_relaxed(cnt + 1, 1);
+  }
+  return true;
 }
 
 // ---------------------------------------------------------- statistics epilogue
@@ -649,6 +875,18 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
       }
     }
   }
+  if (SWAP && !LOCALT && P.tsplit && cta < P.tchunks && threadIdx.x == 64) {
+    // the same hints for the split-K adapter's chunk (down matrix and tokens)
+    int p = 0;
+    while (P.tch0[p + 1] <= cta) ++p;
+    const CUtensorMap* mp = maps.m[p];
+    const int kb0 = (cta - P.tch0[p]) * P.tkpc;
+    const int kb1 = min((P.pb[p].d_in + kBK - 1) / kBK, kb0 + P.tkpc);
+    for (int kb = kb0; kb < kb1; ++kb) {
+      for (int t = 0; t * kBM < P.pb[p].r; ++t) ptx::tma_prefetch_l2_2d(&mp[MAP_A], kb * kBK, t * kBM);
+      ptx::tma_prefetch_l2_2d(&mp[MAP_X], kb * kBK, 0);
+    }
+  }
   // Everything below may read what the previous launch wrote.
   ptx::grid_dependency_wait();
 
@@ -720,7 +958,10 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
               // them.  Should the wait give up, T is loaded all the same (the
               // stage must complete before the CTA may exit) and the launch aborts.
               bool ok = true;
-              if (SWAP) {
+              if (SWAP && P.tsplit) {
+                ok = wait_count(P.tflag + pb.tflag0 + 1, P.tch0[f.prob + 1] - P.tch0[f.prob],
+                                kWaitLimitNs);
+              } else if (SWAP) {
                 for (int j = 0; j < pb.ttiles && ok; ++j)
                   ok = wait_flag(P.tflag + pb.tflag0 + j, kWaitLimitNs);
               } else {
@@ -846,6 +1087,13 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
         for (int m = et; m < P.M; m += kEpiThreads)
           gate_s[p * int(kSwapMaxRows) + m] = P.pb[p].r > 0 ? P.pb[p].gate[m] : uint8_t(0);
       epi_sync();
+      if constexpr (kPreMerge && !LOCALT) {
+        if (P.tsplit && cta < P.tchunks &&
+            !tsplit_run(P, maps, cta, et, gate_s, reinterpret_cast<float4*>(gate_s + kGateOnlyBytes),
+                        reinterpret_cast<uint8_t*>(staging), staging_bytes<BNMAX, LOCALT>(), stg_bar,
+                        stg_phase))
+          *abort_flag = 1;
+      }
     }
     if (SWAP && STATS) {
       for (int m = et; m < P.M; m += kEpiThreads) xd_s[m] = row_draft_token(P.pb[0], m);
@@ -1159,10 +1407,11 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
 
 // Clears the schedule's flags once the previous launch in the stream has
 // finished, letting the projection kernel that follows start right away.
-__global__ void sync_reset_kernel(int* __restrict__ sync, int n) {
+// (16-byte aligned, n16 16-byte words)
+__global__ void sync_reset_kernel(int4* __restrict__ sync, int n16) {
   if (threadIdx.x == 0) ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) sync[i] = 0;
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) sync[i] = make_int4(0, 0, 0, 0);
 }
 
 __global__ void cast_f32_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
@@ -1210,6 +1459,7 @@ struct Layout {
   Params P;
   int tflags;
   size_t off_t[kMaxLoraProblems];
+  size_t off_tpart;  // split-K adapter partials
   size_t off_partial, off_sync, sync_bytes;
   size_t off_cast[kMaxLoraProblems][4];  // fp32 mode: bf16 copies of x, W, A, B
   size_t bytes;
@@ -1222,10 +1472,11 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   std::memset(&L, 0, sizeof(L));
   Params& P = L.P;
   P.M = int(M);
-  // Decode-sized M swaps the operands (weights fill the 128-row MMA side).
-  // A short launch (little weight to stream) cannot hide the latency of a
-  // shared T, so each piece then computes its own share of the adapter
-  // (ranks up to 128); a long launch computes T once per T tile.
+  // Decode-sized M swaps the operands (weights fill the 128-row MMA side)
+  // and computes the adapter input T by split K in the epilogue warps, which
+  // leaves the weight stream alone; larger M computes T once per T tile in
+  // the down section.  (The per-piece adapter, LOCALT, remains for launches
+  // built without the split-K adapter.)
   P.swap = M <= kSwapMaxRows ? 1 : 0;
   int64_t wbytes = 0;
   bool small_rank = true, any_rank = false;
@@ -1234,7 +1485,17 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     small_rank = small_rank && pr[p].rank <= kMaxLocalRank;
     any_rank = any_rank || pr[p].rank > 0;
   }
-  P.localt = (P.swap && any_rank && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
+  // (the split-K adapter needs a CTA per adapted problem at least)
+  int n_adapted = 0;
+  int64_t swap_kb = 0;
+  for (int p = 0; p < n; ++p) {
+    n_adapted += pr[p].rank > 0;
+    swap_kb += ((pr[p].d_out + kBM - 1) / kBM) *
+               ((pr[p].rank + kBK - 1) / kBK + (pr[p].d_in + kBK - 1) / kBK);
+  }
+  const int64_t g_swap = std::max<int64_t>(1, std::min<int64_t>(std::min(sms, kMaxGrid), swap_kb / 4));
+  P.tsplit = (kSplitKAdapter && M <= kSplitKMaxRows && any_rank && n_adapted <= g_swap) ? 1 : 0;
+  P.localt = (!P.tsplit && P.swap && any_rank && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
   P.out_f32 = dtype == UNO_F32;
   const int bn_tok = pick_bn(M);
 
@@ -1245,11 +1506,13 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   int64_t total_kb = 0, tiles_total = 0;
   for (int p = 0; p < n; ++p) {
     Prob& b = P.pb[p];
+    b.d_in = int(pr[p].d_in);
     b.d_out = int(pr[p].d_out);
     b.r = int(pr[p].rank);
     b.scale = pr[p].rank > 0 ? pr[p].alpha / float(pr[p].rank) : 0.f;
     b.tflag0 = tflags;
-    if (pr[p].rank == 0 || P.localt) continue;
+    if (P.tsplit && pr[p].rank > 0) tflags += 2;  // chunks in, slices out
+    if (pr[p].rank == 0 || P.localt || P.tsplit) continue;
     Phase f{};
     f.prob = p;
     f.down = 1;
@@ -1313,6 +1576,30 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   // One CTA per SM, at least 4 K-blocks each.
   const int G = int(std::max<int64_t>(1, std::min<int64_t>(std::min(sms, kMaxGrid), total_kb / 4)));
   P.grid = G;
+  // Split-K adapter: chunks of tkpc K-blocks, no more chunks than CTAs.
+  if (P.tsplit) {
+    int64_t kbt = 0;
+    for (int p = 0; p < n; ++p)
+      if (pr[p].rank > 0) kbt += (pr[p].d_in + kBK - 1) / kBK;
+    int kpc = int(std::max<int64_t>(1, (kbt + G - 1) / G));
+    while (true) {
+      int c = 0;
+      for (int p = 0; p < n; ++p) {
+        P.tch0[p] = c;
+        if (pr[p].rank > 0) c += int(((pr[p].d_in + kBK - 1) / kBK + kpc - 1) / kpc);
+      }
+      P.tch0[n] = c;
+      if (c <= G) break;
+      ++kpc;
+    }
+    for (int p = n + 1; p <= kMaxLoraProblems; ++p) P.tch0[p] = P.tch0[n];
+    P.tkpc = kpc;
+    P.tbn = bn_tok;
+    P.tchunks = P.tch0[n];
+    int max_rank = 0;
+    for (int p = 0; p < n; ++p) max_rank = std::max(max_rank, int(pr[p].rank));
+    P.tpart_stride = int64_t(align_up(size_t(M) * size_t(max_rank), 64));
+  }
 
   // Large M: whole tiles in data-parallel waves (tile t to CTA t % G, so the
   // tiles in flight at once share their operands in L2).  Merging a split
@@ -1397,6 +1684,8 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     L.off_t[p] = o;
     o = align_up(o + size_t(M) * size_t(pr[p].rank) * 2, 256);
   }
+  L.off_tpart = o;
+  if (P.tsplit) o = align_up(o + size_t(P.tchunks) * size_t(P.tpart_stride) * sizeof(float), 256);
   L.off_partial = o;
   o = align_up(o + size_t(G) * 2 * size_t(bnmax) * kBM * sizeof(float), 256);
   L.off_sync = o;
@@ -1525,6 +1814,25 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
   // 11: the partial slots hold a tile of the widest phase
   for (int p = 0; p < P.ph1[1]; ++p)
     if (P.ph[p].bn > P.bnmax) return 11;
+  // 12: split-K adapter only in decode order and without T tiles; its chunks,
+  // in problem order and at most one per CTA, cover every adapted problem's
+  // K-blocks; its partials fit their workspace region
+  if (P.tsplit) {
+    if (!P.swap || P.localt || sec_total[kDown] > 0 || P.tkpc < 1 || P.bnmax > 64 ||
+        P.tbn != P.bnmax || M > P.tbn)
+      return 12;
+    if (P.tch0[0] != 0 || P.tch0[n] != P.tchunks || P.tchunks > G) return 12;
+    int64_t max_r = 0;
+    for (int p = 0; p < n; ++p) {
+      const int64_t nkb = (pr[p].d_in + kBK - 1) / kBK;
+      const int64_t want = pr[p].rank > 0 ? (nkb + P.tkpc - 1) / P.tkpc : 0;
+      if (P.tch0[p + 1] - P.tch0[p] != want) return 12;
+      max_r = std::max<int64_t>(max_r, pr[p].rank);
+    }
+    if (P.tpart_stride < M * max_r || P.tpart_stride % 4 ||
+        L.off_tpart + size_t(P.tchunks) * size_t(P.tpart_stride) * sizeof(float) > L.off_partial)
+      return 12;
+  }
   return 0;
 }
 
@@ -1584,6 +1892,7 @@ int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w,
   if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
   Params& P = L.P;
   P.partial = reinterpret_cast<float*>(w + L.off_partial);
+  P.tpart = reinterpret_cast<float*>(w + L.off_tpart);
   P.ready = reinterpret_cast<int*>(w + L.off_sync);
   P.tflag = P.ready + 2 * P.grid;
   std::memset(&maps, 0, sizeof(maps));
@@ -1600,6 +1909,7 @@ int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w,
     b.y = q.y;
     b.t = w + L.off_t[p];
     b.gate = q.gate;
+
     if (epi) {
       b.f32out = epi->f32out;
       b.st_store = epi->stats_store;
@@ -1716,8 +2026,9 @@ int launch_linear(int n, const uno_lora_problem* pr, int64_t M, int dtype, void*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sync_reset_kernel, reinterpret_cast<int*>(w + L.off_sync),
-                           int(L.sync_bytes / sizeof(int))) != cudaSuccess)
+    if (reinterpret_cast<uintptr_t>(w + L.off_sync) & 15u) return UNO_ERR_WORKSPACE;
+    if (cudaLaunchKernelEx(&cfg, sync_reset_kernel, reinterpret_cast<int4*>(w + L.off_sync),
+                           int(L.sync_bytes / 16)) != cudaSuccess)
       return UNO_ERR_CUDA;
   }
   cudaError_t e;

@@ -164,6 +164,20 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                : "memory");
 }
 
+// Warp-level mma.sync m16n8k16 (bf16 inputs, fp32 accumulate) for small side
+// products.  Fragments as the PTX ISA lays them out, with g = lane / 4 and
+// t = lane % 4: A (16 x 16, row-major) a0 = A[g][2t..2t+1], a1 = A[g+8][2t..],
+// a2 = A[g][2t+8..], a3 = A[g+8][2t+8..]; B (16 x 8, K x N) b0 = B[2t..2t+1][g],
+// b1 = B[2t+8..][g]; D (16 x 8) d0,d1 = D[g][2t..2t+1], d2,d3 = D[g+8][2t..].
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Shared-memory matrix descriptor for a K-major bf16 tile stored as TMA writes
 // it with 128-byte swizzling: rows of 64 elements (128 B), 8-row groups
 // 1024 B apart.  Fields: start address >> 4 (bits 0-13), leading byte offset

@@ -42,6 +42,8 @@ def _ref(pr, rows=None):
     (256, 1024, 520, 64, 128.0, torch.bfloat16, 16),   # large-M order, fewer tiles than CTAs
     (300, 512, 1000, 128, 256.0, torch.bfloat16, 16),  # non-swap path, ragged M and N
     (40, 64, 64, 8, 16.0, torch.bfloat16, 16),         # single K-block
+    (48, 512, 256, 256, 512.0, torch.bfloat16, 16),    # rank 256: two 128-row passes of the split-K adapter
+    (32, 16384, 64, 256, 512.0, torch.bfloat16, 16),   # split-K adapter chunks staged in several rounds
 ])
 def test_lora_parity(M, d_in, d_out, r, alpha, dtype, block):
     pr = inputs.lora_problem(M, d_in, d_out, r, alpha, dtype=dtype, block=block,
