@@ -57,7 +57,8 @@ def _gpu(pr, draft, mode):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("Bn,K,V,d,Kp", [(2, 4, 1000, 256, None), (3, 5, 4104, 512, 6),
-                                          (70, 4, 2048, 256, None), (9, 16, 8192, 1024, 17)])
+                                          (70, 4, 2048, 256, None), (9, 16, 8192, 1024, 17),
+                                          (6, 12, 4096, 512, 13)])  # 150 rows: just above the weights-as-A limit
 def test_lm_head_parity(mode, Bn, K, V, d, Kp):
     pr = inputs.lm_head_problem(Bn, K, V, d, Kp=Kp, sigma=1.0)
     draft = _drafts(pr)
