@@ -62,6 +62,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -1527,25 +1528,34 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     tl[nt++] = f;
   }
   const int n_down = nt;
-  // Large M: 256-wide output tiles, or 128-wide ones when those fill the
-  // waves of whole tiles better.  A 128-wide tile moves 32 KB of operands
-  // per 128 output columns and K-block against 48 KB per 256, and the
-  // mainloop is bound by that traffic, so its work counts 4/3.
+  // Large M: 256-wide output tiles, or 128-wide ones when those cost less.
+  // The mainloop is bound by operand traffic (a 128 x 64 token tile plus bn
+  // rows of weights per K-block), so a launch's cost is counted per CTA in
+  // those bytes: whole waves of tiles when there are at least as many tiles
+  // as CTAs (data-parallel order); otherwise (stream-K) an even share of all
+  // tiles' bytes plus the merge of the split tiles' fp32 partials, weighted
+  // four times their bytes (measured: a merge costs L2 round trips, not only
+  // bandwidth -- at 256 rows the split launches took 43 us with 128-wide
+  // tiles against 68 us with 256-wide ones).
   int bn_large = 256;
   if (!P.swap) {
-    auto wave_cost = [&](int bn) {
-      int64_t tiles = 0, work = 0;
-      for (int i = 0; i < n_down; ++i) tiles += tl[i].tiles;
-      for (int p = 0; p < n; ++p) {
-        const int64_t t = ((M + kBM - 1) / kBM) * ((pr[p].d_out + bn - 1) / bn);
-        tiles += t;
-        work += t * ((pr[p].d_in + kBK - 1) / kBK) * bn;
+    auto cost = [&](int bn) {
+      double tiles = 0, bytes = 0;
+      for (int i = 0; i < n_down; ++i) {
+        tiles += tl[i].tiles;
+        bytes += double(tl[i].tiles) * tl[i].nkb * (double(kABytes) + tl[i].bn * 128.0);
       }
-      const int64_t G0 = std::min(sms, kMaxGrid);
-      return tiles >= G0 ? ((tiles + G0 - 1) / G0) * G0 * (work / tiles) : INT64_MAX;
+      for (int p = 0; p < n; ++p) {
+        const double t = double((M + kBM - 1) / kBM) * double((pr[p].d_out + bn - 1) / bn);
+        tiles += t;
+        bytes += t * double((pr[p].rank + kBK - 1) / kBK + (pr[p].d_in + kBK - 1) / kBK) *
+                 (double(kABytes) + bn * 128.0);
+      }
+      const double G0 = double(std::min(sms, kMaxGrid));
+      if (tiles >= G0) return std::ceil(tiles / G0) * (bytes / tiles);
+      return bytes / G0 + 4.0 * (G0 - tiles) / tiles * (double(kBM) * bn * 4.0);
     };
-    const int64_t c128 = wave_cost(128), c256 = wave_cost(256);
-    if (c128 != INT64_MAX && (c256 == INT64_MAX || c128 / 3 * 4 < c256)) bn_large = 128;
+    if (cost(128) < cost(256)) bn_large = 128;
   }
   for (int p = 0; p < n; ++p) {
     Phase f{};
