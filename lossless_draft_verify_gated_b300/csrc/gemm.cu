@@ -1689,6 +1689,18 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     P.lo[kMain][c] = std::min(Mn, std::max(P.lo[kMain][c - 1], v));
   }
   P.lo[kMain][G] = Mn;
+  // A boundary inside a tile's adapter K-blocks (the first na of its flat
+  // order) moves back to the tile's start: only the tile's finisher then
+  // runs adapter K-blocks, and no contributor's first piece waits for T.
+  for (int c = 1; c < G; ++c) {
+    const int64_t k = P.lo[kMain][c];
+    if (k <= 0 || k >= Mn || t_fin[c]) continue;  // (a T tile's finisher keeps no main work)
+    int p = P.ph0[kMain];
+    while (p + 1 < P.ph1[kMain] && P.ph[p + 1].kb_start <= k) ++p;
+    const Phase& f = P.ph[p];
+    const int64_t ts = f.kb_start + (k - f.kb_start) / f.nkb * f.nkb;
+    if (k > ts && k < ts + f.na) P.lo[kMain][c] = std::max(P.lo[kMain][c - 1], ts);
+  }
   size_t o = 0;
   for (int p = 0; p < n; ++p) {
     L.off_t[p] = o;
