@@ -581,7 +581,7 @@ VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   // Statistics pass: one wave of kStatsCtasPerSm CTAs of 256 threads per SM;
   // split rows only while each chunk keeps at least 2048 logits.
   const int64_t target = int64_t(sms) * kStatsCtasPerSm;
-  int64_t s = pl.rows > 0 ? (target + pl.rows - 1) / pl.rows : 1;
+  int64_t s = pl.rows > 0 ? target / pl.rows : 1;  // (rounded down: no second, nearly empty wave)
   s = std::max<int64_t>(1, std::min<int64_t>(s, (V + 2047) / 2048));
   int64_t chunk = (V + s - 1) / s;
   chunk = (chunk + 3) & ~int64_t(3);
