@@ -29,6 +29,8 @@ struct VerifyPlan {
   int64_t chunk;     // elements per chunk (multiple of 4)
   int race_splits;   // vocab chunks per sequence in the resampling race
   int64_t race_chunk;
+  int icdf_splits;   // the same for the inverse-CDF resample (smaller chunks: the
+  int64_t icdf_chunk;  // last CTA searches one of them for the crossing)
   size_t off_stats, off_gather, off_race, off_count, bytes;
 };
 VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms);

@@ -594,10 +594,17 @@ VerifyPlan plan_verify(int64_t Bn, int64_t K, int64_t Kp, int64_t V, int sms) {
   s2 = std::max<int64_t>(1, std::min<int64_t>(s2, (V + 1023) / 1024));
   pl.race_chunk = (V + s2 - 1) / s2;
   pl.race_splits = int((V + pl.race_chunk - 1) / pl.race_chunk);
+  // Inverse CDF: the same, but chunks of at most 8192 entries, so that the
+  // last CTA's search of the chunk holding the crossing stays short.
+  const int64_t s3 = std::min<int64_t>(std::max<int64_t>(s2, (V + 8191) / 8192), (V + 1023) / 1024);
+  pl.icdf_chunk = (V + s3 - 1) / s3;
+  pl.icdf_splits = int((V + pl.icdf_chunk - 1) / pl.icdf_chunk);
   pl.off_stats = 0;
   pl.off_gather = align_up(pl.off_stats + size_t(pl.rows) * pl.splits * sizeof(float2), 256);
   pl.off_race = align_up(pl.off_gather + size_t(pl.rows) * sizeof(float), 256);
-  pl.off_count = align_up(pl.off_race + size_t(Bn) * pl.race_splits * sizeof(RacePart), 256);
+  pl.off_count = align_up(pl.off_race + size_t(Bn) * std::max(pl.race_splits, pl.icdf_splits) *
+                                            sizeof(RacePart),
+                          256);
   pl.bytes = align_up(pl.off_count + size_t(Bn) * sizeof(int), 256);
   return pl;
 }
@@ -633,9 +640,12 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
                      : cudaLaunchKernelEx(&cfg, verify_stats_kernel<false>, p, q, draft, K, Kp, V,
                                           pl.splits, pl.chunk, inv_t, part, gathered, counter);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(unsigned(Bn * pl.race_splits));
+  const bool icdf = mode == kInverseCdf;
+  const int rs = icdf ? pl.icdf_splits : pl.race_splits;
+  const int64_t rc = icdf ? pl.icdf_chunk : pl.race_chunk;
+  cfg.gridDim = dim3(unsigned(Bn * rs));
   e = ex ? cudaLaunchKernelEx(&cfg, verify_finish_kernel<true>, p, q, draft, u_acc, u_res, K, Kp, V,
-                              pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
+                              pl.splits, rs, rc, inv_t, mode,
                               (const float2*)part, (const float*)gathered, rpart, counter, n_acc,
                               out_tokens, n_emit, status)
          : cudaLaunchKernelEx(&cfg, verify_finish_kernel<false>, p, q, draft, u_acc, u_res, K, Kp,
