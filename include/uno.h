@@ -106,8 +106,9 @@ enum {
  * Requirements: M >= 0, d_in >= 1, d_out >= 1, rank in [0, 256], d_in,
  * d_out and rank multiples of 8; alpha finite.  rank == 0 gives x.W^T.
  * Residency: the kernel is persistent (one CTA per SM) and some CTAs wait,
- * with a 2-second limit, for partial sums that later-started CTAs of the
- * same launch publish.  When other work keeps SMs from this launch (another
+ * with a 2-second limit, for partial sums that other CTAs of the same launch
+ * publish (of output tiles and, for up to 64 rows, of the adapter input
+ * x.A^T, which the CTAs compute by splitting d_in).  When other work keeps SMs from this launch (another
  * stream's long kernel, an MPS or green-context SM limit) such a wait can run
  * out; the CTA then skips its output tile and sets bit 0 of the device error
  * word.  y is therefore defined only when uno_device_error() reads 0 after
@@ -161,7 +162,8 @@ typedef struct {
  * uno_gated_lora_linear_batched would use on a GPU with `sms` SMs and checks
  * its invariants -- the grid fits one CTA per SM, every section's K-blocks
  * are partitioned over the CTAs in order, a split T tile's finisher takes no
- * other work, the workspace regions fit.  Returns 0 when all hold, a positive
+ * other work, the adapter's d_in chunks cover every adapted problem with at
+ * most one chunk per CTA, the workspace regions fit.  Returns 0 when all hold, a positive
  * invariant number otherwise, or UNO_ERR_ARG / UNO_ERR_UNSUPPORTED for
  * arguments the projection itself would refuse (pointers are not read). */
 int uno_lora_plan_check(int n, const uno_lora_problem *problems, int64_t M, int dtype, int sms);
