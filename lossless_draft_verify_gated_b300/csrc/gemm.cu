@@ -468,7 +468,15 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
     const float gs = f.down ? float(pb.gate[m]) * pb.scale : 1.f;
     if (!f.down && (P.out_f32 || pb.f32out)) {
       float* d = static_cast<float*>(pb.y) + int64_t(m) * ncols;
-      if (n0 + 16 <= ncols) {  // ncols and n0 are multiples of 8: 16-byte stores
+      if (n0 + 16 <= ncols && (reinterpret_cast<uintptr_t>(d + n0) & 31u) == 0) {
+        // two 256-bit stores (full 32-byte sectors)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d + n0 + 8 * h),
+                       "f"(v[8 * h]), "f"(v[8 * h + 1]), "f"(v[8 * h + 2]), "f"(v[8 * h + 3]),
+                       "f"(v[8 * h + 4]), "f"(v[8 * h + 5]), "f"(v[8 * h + 6]), "f"(v[8 * h + 7])
+                       : "memory");
+      } else if (n0 + 16 <= ncols) {  // ncols and n0 are multiples of 8: 16-byte stores
         float4* d4 = reinterpret_cast<float4*>(d + n0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -485,8 +493,15 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
         w[j] = *reinterpret_cast<uint32_t*>(&h);
       }
       uint4* d = reinterpret_cast<uint4*>(dst16 + int64_t(m) * ncols + n0);
-      d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      // a lane's 16 outputs are one 32-byte sector: one 256-bit store when aligned
+      if ((reinterpret_cast<uintptr_t>(d) & 31u) == 0) {
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+      } else {
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j)
