@@ -162,7 +162,8 @@ typedef struct {
  * uno_gated_lora_linear_batched would use on a GPU with `sms` SMs and checks
  * its invariants -- the grid fits one CTA per SM, every section's K-blocks
  * are partitioned over the CTAs in order, a split T tile's finisher takes no
- * other work, the adapter's d_in chunks cover every adapted problem with at
+ * other work (decode order) or a split T tile's pieces are whole CTA ranges
+ * in consecutive CTAs (token-rows order), the adapter's d_in chunks cover every adapted problem with at
  * most one chunk per CTA, the workspace regions fit.  Returns 0 when all hold, a positive
  * invariant number otherwise, or UNO_ERR_ARG / UNO_ERR_UNSUPPORTED for
  * arguments the projection itself would refuse (pointers are not read). */

@@ -165,7 +165,9 @@ struct Params {
   int64_t lo[2][kMaxGrid + 1];  // CTA c owns K-blocks [lo[s][c], lo[s][c+1]) of section s
   float* partial;  // [grid][2][bnmax * 128], layout [column/4][row][4]
   int* ready;      // [2][grid]: the first piece of CTA c in section s left its partial
-  int* tflag;      // [T tiles]: the rows of T of the tile are written
+  int* tflag;      // [T tiles]: the rows of T of the tile are written (a count of
+                   // slices for a split T tile of the token-rows order)
+  int* tcnt;       // [T tiles] (token-rows order): pieces of a split T tile whose partial is in
 };
 
 // Shared memory (per CTA): a ring of STAGES stages, each one K-block of the
@@ -324,6 +326,23 @@ __device__ __forceinline__ int owner_of(const Params& P, int sec, int64_t k) {
     if (P.lo[sec][m] <= k) a = m; else b = m - 1;
   }
   return a;
+}
+
+// Token-rows order: the CTAs [c0, c0 + np) that hold the pieces of T tile
+// `ta` of problem `prob` in the down section, one piece each (np = 1, c0 = -1
+// for a T tile that is not split).
+__device__ __forceinline__ void t_tile_span(const Params& P, int prob, int ta, int& c0, int& np) {
+  c0 = -1;
+  np = 1;
+  for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
+    const Phase& f = P.ph[p];
+    const int t = ta - f.tile0;
+    if (f.prob != prob || t < 0 || t >= f.tiles) continue;
+    const int64_t kb0 = f.kb_start + int64_t(t) * f.nkb;
+    c0 = owner_of(P, kDown, kb0);
+    np = owner_of(P, kDown, kb0 + f.nkb - 1) - c0 + 1;
+    return;
+  }
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -981,7 +1000,9 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
                 for (int j = 0; j < pb.ttiles && ok; ++j)
                   ok = wait_flag(P.tflag + pb.tflag0 + j, kWaitLimitNs);
               } else {
-                ok = wait_flag(P.tflag + pb.tflag0 + ta, kWaitLimitNs);
+                int c0t, np;
+                t_tile_span(P, f.prob, ta, c0t, np);
+                ok = wait_count(P.tflag + pb.tflag0 + ta, np, kWaitLimitNs);
               }
               if (!ok) *abort_flag = 1;
               fence_proxy_async();
@@ -1127,7 +1148,9 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
         tile_coords(f, g.tile, ta, tb);
         const int acc = seg % kAcc, use = seg / kAcc;
         const bool whole = g.s == g.tstart && g.e == g.tend;
-        const bool finisher = !whole && g.s == g.tstart;
+        // a piece of a split T tile in token-rows order (see below)
+        const bool tslice = !SWAP && f.down && !whole;
+        const bool finisher = !whole && !tslice && g.s == g.tstart;
         const int c1 = finisher ? owner_of(P, sec, g.tend - 1) : cta;
         bool fail = false;
         // The tile's final values leave through emit (16 columns at a time, in
@@ -1272,6 +1295,86 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
               emit(c0, v);
             }
             emit_end();
+          } else if (tslice) {
+            // Split T tile (token-rows order): every piece leaves its partial
+            // and counts in; once all np pieces are in, piece i sums slice i of
+            // the tile (8-column units) over the pieces in CTA order -- the
+            // order in which one finisher would add them -- and stores it as
+            // T' = bf16(gate * scale * T).  The merge and the publication are
+            // spread over the pieces; consumers wait for np slices.
+            int c0t, np;
+            t_tile_span(P, f.prob, ta, c0t, np);
+            float4* dst = reinterpret_cast<float4*>(P.partial + (size_t(cta) * 2 + sec) * kSlot);
+            for (int c0 = 0; c0 < f.bn; c0 += 16) {
+              float v[16];
+              tmem_ld16f(tq + c0, v);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                __stcg(dst + ((c0 >> 2) + i) * kBM + row,
+                       make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            }
+            // the accumulator is free for the CTA's next piece at once
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+            epi_sync();
+            int* cnt = P.tcnt + pb.tflag0 + ta;
+            bool ok = true;
+            if (et == 0) {
+              fence_acq_rel_gpu();
+              red_add_relaxed(cnt, 1);
+              ok = wait_count(cnt, np, kWaitLimitNs);
+            }
+            // thread 0's acquire, then the barrier, order the loads below
+            // after every piece's partial
+            if (epi_sync_or(!ok)) {
+              *abort_flag = 1;
+              goto done;
+            }
+            const int nu = pb.r >> 3;
+            const int pi = cta - c0t;
+            const int u0 = pi * nu / np, u1 = (pi + 1) * nu / np;
+            const int m = ta * kBM + row;
+            const float gs = m < P.M ? float(pb.gate[m]) * pb.scale : 0.f;
+            for (int u = u0; u < u1; ++u) {
+              float sum[8];
+              for (int k0 = 0; k0 < np; k0 += 4) {
+                float4 t[4][2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float4* src = reinterpret_cast<const float4*>(
+                      P.partial + (size_t(c0t + (k0 + k < np ? k0 + k : 0)) * 2 + sec) * kSlot);
+                  t[k][0] = __ldcg(src + (2 * u) * kBM + row);
+                  t[k][1] = __ldcg(src + (2 * u + 1) * kBM + row);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  if (k0 + k >= np) break;
+                  const float x[8] = {t[k][0].x, t[k][0].y, t[k][0].z, t[k][0].w,
+                                      t[k][1].x, t[k][1].y, t[k][1].z, t[k][1].w};
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) sum[j] = (k0 + k == 0) ? x[j] : sum[j] + x[j];
+                }
+              }
+              if (m < P.M) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(sum[2 * j] * gs, sum[2 * j + 1] * gs);
+                  w[j] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pb.t) + int64_t(m) * pb.r + 8 * u) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+            // T' is read next by TMA in other CTAs: async-proxy fence, then
+            // the release of this slice
+            fence_proxy_async();
+            epi_sync();
+            if (et == 0) {
+              fence_acq_rel_gpu();
+              red_add_relaxed(P.tflag + pb.tflag0 + ta, 1);
+            }
           } else if (!finisher) {
             // contributor: leave the piece as a partial and raise this CTA's flag
             float4* dst = reinterpret_cast<float4*>(P.partial + (size_t(cta) * 2 + sec) * kSlot);
@@ -1388,15 +1491,17 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
             }
             emit_end();
           }
-          // the accumulator may be reused
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+          if (!tslice) {
+            // the accumulator may be reused
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+          }
           // A partial (read by the finisher's bulk copies) or a finished T tile
           // (read by TMA in other CTAs) is published with a release: every
           // thread orders its stores before the async proxy, the barrier
           // orders them before thread 0, whose fence and flag store release them.
-          const bool publish_partial = !whole && !finisher;
+          const bool publish_partial = !whole && !finisher && !tslice;
           const bool publish_t = f.down && (whole || finisher);
           if (publish_partial || publish_t) {
             fence_proxy_async();
@@ -1664,24 +1769,46 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   // (one round of bulk copies); at large M, where T tiles are many and cheap,
   // whole tiles up to half a CTA's share.
   int Gd = 0;
-  if (D > 0) {
+  if (D > 0 && P.swap) {
     const int64_t slots =
         bnmax <= 64 ? std::max<int64_t>(1, kSharedTStaging / (int64_t(bnmax) * kBM * 4)) : 16;
     int64_t kd = std::max<int64_t>(4, (max_down_nkb + slots - 1) / slots);
     // a long T tile (down projection of a wide input) may take two rounds:
     // shorter pieces finish T sooner than one more round of copies costs
-    if (P.swap && kd > 16) kd = (kd + 1) / 2;
-    if (!P.swap) kd = std::max<int64_t>(kd, std::min<int64_t>(max_down_nkb, Wt / G / 2));
+    if (kd > 16) kd = (kd + 1) / 2;
     Gd = int(std::max<int64_t>(1, std::min<int64_t>(G, (D + kd - 1) / kd)));
   }
   for (int c = 0; c <= G; ++c) P.lo[kDown][c] = c <= Gd && Gd > 0 ? int64_t(c) * D / Gd : D;
+  if (D > 0 && !P.swap) {
+    // Token-rows order: every T tile in pieces of about a quarter of a CTA's
+    // share of K-blocks (at least 4), one piece per CTA, so that T is
+    // complete early; the pieces merge and publish the tile together, each a
+    // slice of it, so that more pieces cost no longer merge.
+    int64_t kd = std::max<int64_t>(4, (Wt / G + 3) / 4);
+    auto pieces = [&](int64_t k) {
+      int64_t n_pc = 0;
+      for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p)
+        n_pc += int64_t(P.ph[p].tiles) * ((P.ph[p].nkb + k - 1) / k);
+      return n_pc;
+    };
+    while (pieces(kd) > G) ++kd;
+    int c = 0;
+    for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
+      const Phase& f = P.ph[p];
+      const int64_t np = (f.nkb + kd - 1) / kd;
+      for (int t = 0; t < f.tiles; ++t)
+        for (int64_t i = 0; i < np; ++i)
+          P.lo[kDown][c++] = f.kb_start + int64_t(t) * f.nkb + i * f.nkb / np;
+    }
+    for (; c <= G; ++c) P.lo[kDown][c] = D;
+  }
   // Main section: CTA c's range ends where the first c+1 CTAs have streamed
-  // (c+1)/G of the section's K-blocks, down ones included -- except that a
-  // CTA finishing a split T tile (it waits for and merges the tile's pieces,
-  // then publishes T) takes no main work, which the others share.
+  // (c+1)/G of the section's K-blocks, down ones included -- except that, in
+  // decode order, a CTA finishing a split T tile (it waits for and merges the
+  // tile's pieces, then publishes T) takes no main work, which the others share.
   bool t_fin[kMaxGrid + 1] = {};
   int n_fin = 0;
-  for (int c = 0; c < G && D > 0; ++c) {
+  for (int c = 0; c < G && D > 0 && P.swap; ++c) {
     const int64_t lo0 = P.lo[kDown][c], hi0 = P.lo[kDown][c + 1];
     if (lo0 >= hi0) continue;
     // the CTA's last down piece starts a T tile that continues beyond it
@@ -1726,7 +1853,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   L.off_partial = o;
   o = align_up(o + size_t(G) * 2 * size_t(bnmax) * kBM * sizeof(float), 256);
   L.off_sync = o;
-  L.sync_bytes = align_up((2 * size_t(G) + size_t(tflags)) * sizeof(int), 256);
+  L.sync_bytes = align_up((2 * size_t(G) + 2 * size_t(tflags)) * sizeof(int), 256);
   o += L.sync_bytes;
   if (dtype == UNO_F32) {
     for (int p = 0; p < n; ++p) {
@@ -1827,9 +1954,10 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
   }
   // 7: a per-piece adapter needs no T tiles
   if (P.localt && sec_total[kDown] > 0) return 7;
-  // 8: a CTA that finishes a split T tile has no main work (unless all do)
+  // 8: (decode order) a CTA that finishes a split T tile has no main work
+  // (unless all do)
   int n_fin = 0, n_fin_busy = 0;
-  for (int c = 0; c < G; ++c) {
+  for (int c = 0; c < G && P.swap; ++c) {
     const int64_t lo0 = P.lo[kDown][c], hi0 = P.lo[kDown][c + 1];
     if (lo0 >= hi0) continue;
     for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
@@ -1844,6 +1972,28 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
     }
   }
   if (n_fin_busy > 0 && n_fin < G) return 8;
+  // 13: (token-rows order) the down section's CTA ranges are pieces of single
+  // T tiles, one per CTA, with every piece of a tile in consecutive CTAs,
+  // and the T counters fit the sync area
+  if (!P.swap && sec_total[kDown] > 0) {
+    int c = 0;
+    for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
+      const Phase& f = P.ph[p];
+      for (int t = 0; t < f.tiles; ++t) {
+        const int64_t kb0 = f.kb_start + int64_t(t) * f.nkb, kb1 = kb0 + f.nkb;
+        if (P.lo[kDown][c] != kb0) return 13;
+        while (c < G && P.lo[kDown][c + 1] < kb1) {
+          if (P.lo[kDown][c + 1] <= P.lo[kDown][c]) return 13;
+          ++c;
+        }
+        if (c >= G || P.lo[kDown][c + 1] != kb1) return 13;
+        ++c;
+      }
+    }
+    for (; c < G; ++c)
+      if (P.lo[kDown][c] != P.lo[kDown][c + 1]) return 13;
+    if ((2 * size_t(G) + 2 * size_t(L.tflags)) * sizeof(int) > L.sync_bytes) return 13;
+  }
   // 9: decode order only for decode-sized M
   if (P.swap != (M <= kSwapMaxRows ? 1 : 0)) return 9;
   // 10: workspace regions in order and inside the total
@@ -1932,6 +2082,7 @@ int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w,
   P.tpart = reinterpret_cast<float*>(w + L.off_tpart);
   P.ready = reinterpret_cast<int*>(w + L.off_sync);
   P.tflag = P.ready + 2 * P.grid;
+  P.tcnt = P.tflag + L.tflags;
   std::memset(&maps, 0, sizeof(maps));
   for (int p = 0; p < n; ++p) {
     const uno_lora_problem& q = pr[p];

@@ -44,6 +44,8 @@ def _ref(pr, rows=None):
     (40, 64, 64, 8, 16.0, torch.bfloat16, 16),         # single K-block
     (48, 512, 256, 256, 512.0, torch.bfloat16, 16),    # rank 256: two 128-row passes of the split-K adapter
     (32, 16384, 64, 256, 512.0, torch.bfloat16, 16),   # split-K adapter chunks staged in several rounds
+    (256, 14336, 1024, 128, 256.0, torch.bfloat16, 16),  # long T tiles, each in many pieces (token-rows order)
+    (384, 1024, 512, 256, 512.0, torch.bfloat16, 16),    # rank 256 in token-rows order: 32 slices per T tile
 ])
 def test_lora_parity(M, d_in, d_out, r, alpha, dtype, block):
     pr = inputs.lora_problem(M, d_in, d_out, r, alpha, dtype=dtype, block=block,

@@ -2,9 +2,10 @@
 CPU through the library's own scheduler (uno_lora_plan_check, no GPU): the
 grid fits one CTA per SM, each stream-K section's K-blocks are partitioned
 over the CTAs in order, data-parallel waves cover every tile, a split T
-tile's finisher takes no other work, the workspace regions fit.  The waits
-of the kernel end only if these hold (a split tile's contributors are later
-CTAs, all resident at once)."""
+tile's finisher takes no other work (decode order) or a split T tile's pieces
+are whole ranges of consecutive CTAs (token-rows order), the workspace
+regions fit.  The waits of the kernel end only if these hold (a split tile's
+contributors are later CTAs, all resident at once)."""
 import random
 
 import pytest
