@@ -85,7 +85,8 @@ constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 4 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
-constexpr int kPrefetchKBlocks = 8;  // weight tiles hinted into L2 before the previous launch ends
+constexpr int kPrefetchKBlocks = 8;
+constexpr int64_t kTSliceMaxShare = 160;  // K-blocks a CTA, for T tiles merged by slices  // weight tiles hinted into L2 before the previous launch ends
 constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;
 constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand
 constexpr bool kSplitKAdapter = true;  // decode order: T by split K in the epilogue warps
@@ -148,6 +149,7 @@ struct Params {
   int nprob;           // problems of the launch
   int swap;
   int localt;  // swap path with per-piece adapter
+  int tslice;  // (token-rows order) split T tiles merge and publish by slices
   // Split-K adapter (decode order): the epilogue warps of CTA c < tchunks
   // compute the partial T of chunk c (tkpc K-blocks of one problem's d_in;
   // problem p owns chunks [tch0[p], tch0[p+1])), then reduce a slice of T.
@@ -334,6 +336,7 @@ __device__ __forceinline__ int owner_of(const Params& P, int sec, int64_t k) {
 __device__ __forceinline__ void t_tile_span(const Params& P, int prob, int ta, int& c0, int& np) {
   c0 = -1;
   np = 1;
+  if (!P.tslice) return;  // a split T tile has one finisher, which publishes it
   for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
     const Phase& f = P.ph[p];
     const int t = ta - f.tile0;
@@ -1149,7 +1152,7 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
         const int acc = seg % kAcc, use = seg / kAcc;
         const bool whole = g.s == g.tstart && g.e == g.tend;
         // a piece of a split T tile in token-rows order (see below)
-        const bool tslice = !SWAP && f.down && !whole;
+        const bool tslice = !SWAP && P.tslice && f.down && !whole;
         const bool finisher = !whole && !tslice && g.s == g.tstart;
         const int c1 = finisher ? owner_of(P, sec, g.tend - 1) : cta;
         bool fail = false;
@@ -1768,18 +1771,25 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   // T tile in no more pieces than its finisher's staging area holds at once
   // (one round of bulk copies); at large M, where T tiles are many and cheap,
   // whole tiles up to half a CTA's share.
+  // Token-rows order, split T tiles: merged by slices over their pieces when a
+  // CTA's share of K-blocks is short (the pieces' waits and slice sums are
+  // then what T waits for), else by one finisher that takes no main work
+  // (measured: the down projection at 512 and 1024 rows, 201 and 207 K-blocks
+  // a CTA, took 82 and 123 us that way against 88 and 168 us by slices).
+  P.tslice = (!P.swap && D > 0 && Wt / G <= kTSliceMaxShare) ? 1 : 0;
   int Gd = 0;
-  if (D > 0 && P.swap) {
+  if (D > 0 && !P.tslice) {
     const int64_t slots =
         bnmax <= 64 ? std::max<int64_t>(1, kSharedTStaging / (int64_t(bnmax) * kBM * 4)) : 16;
     int64_t kd = std::max<int64_t>(4, (max_down_nkb + slots - 1) / slots);
     // a long T tile (down projection of a wide input) may take two rounds:
     // shorter pieces finish T sooner than one more round of copies costs
-    if (kd > 16) kd = (kd + 1) / 2;
+    if (P.swap && kd > 16) kd = (kd + 1) / 2;
+    if (!P.swap) kd = std::max<int64_t>(kd, std::min<int64_t>(max_down_nkb, Wt / G / 2));
     Gd = int(std::max<int64_t>(1, std::min<int64_t>(G, (D + kd - 1) / kd)));
   }
   for (int c = 0; c <= G; ++c) P.lo[kDown][c] = c <= Gd && Gd > 0 ? int64_t(c) * D / Gd : D;
-  if (D > 0 && !P.swap) {
+  if (P.tslice) {
     // Token-rows order: every T tile in pieces of about a quarter of a CTA's
     // share of K-blocks (at least 4), one piece per CTA, so that T is
     // complete early; the pieces merge and publish the tile together, each a
@@ -1803,12 +1813,12 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     for (; c <= G; ++c) P.lo[kDown][c] = D;
   }
   // Main section: CTA c's range ends where the first c+1 CTAs have streamed
-  // (c+1)/G of the section's K-blocks, down ones included -- except that, in
-  // decode order, a CTA finishing a split T tile (it waits for and merges the
-  // tile's pieces, then publishes T) takes no main work, which the others share.
+  // (c+1)/G of the section's K-blocks, down ones included -- except that a CTA
+  // finishing a split T tile alone (it waits for and merges the tile's pieces,
+  // then publishes T) takes no main work, which the others share.
   bool t_fin[kMaxGrid + 1] = {};
   int n_fin = 0;
-  for (int c = 0; c < G && D > 0 && P.swap; ++c) {
+  for (int c = 0; c < G && D > 0 && !P.tslice; ++c) {
     const int64_t lo0 = P.lo[kDown][c], hi0 = P.lo[kDown][c + 1];
     if (lo0 >= hi0) continue;
     // the CTA's last down piece starts a T tile that continues beyond it
@@ -1954,10 +1964,10 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
   }
   // 7: a per-piece adapter needs no T tiles
   if (P.localt && sec_total[kDown] > 0) return 7;
-  // 8: (decode order) a CTA that finishes a split T tile has no main work
-  // (unless all do)
+  // 8: (one finisher per split T tile) a CTA that finishes a split T tile
+  // has no main work (unless all do)
   int n_fin = 0, n_fin_busy = 0;
-  for (int c = 0; c < G && P.swap; ++c) {
+  for (int c = 0; c < G && !P.tslice; ++c) {
     const int64_t lo0 = P.lo[kDown][c], hi0 = P.lo[kDown][c + 1];
     if (lo0 >= hi0) continue;
     for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
@@ -1972,10 +1982,11 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
     }
   }
   if (n_fin_busy > 0 && n_fin < G) return 8;
-  // 13: (token-rows order) the down section's CTA ranges are pieces of single
-  // T tiles, one per CTA, with every piece of a tile in consecutive CTAs,
-  // and the T counters fit the sync area
-  if (!P.swap && sec_total[kDown] > 0) {
+  // 13: (T tiles merged by slices) only in token-rows order; the down
+  // section's CTA ranges are pieces of single T tiles, one per CTA, with every
+  // piece of a tile in consecutive CTAs, and the T counters fit the sync area
+  if (P.tslice && (P.swap || sec_total[kDown] == 0)) return 13;
+  if (P.tslice) {
     int c = 0;
     for (int p = P.ph0[kDown]; p < P.ph1[kDown]; ++p) {
       const Phase& f = P.ph[p];
