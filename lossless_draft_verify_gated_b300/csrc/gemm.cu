@@ -65,6 +65,7 @@
 #include <cmath>
 #include <cstring>
 #include <memory>
+#include <atomic>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -85,10 +86,11 @@ constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxPhases = 4 * kMaxLoraProblems;
 constexpr int kMaxGrid = 160;  // CTAs of one launch (one per SM)
-constexpr int kPrefetchKBlocks = 8;
-constexpr int64_t kTSliceMaxShare = 160;  // K-blocks a CTA, for T tiles merged by slices  // weight tiles hinted into L2 before the previous launch ends
+constexpr int kPrefetchKBlocks = 8;  // weight tiles hinted into L2 before the previous launch ends
+constexpr int64_t kTSliceMaxShare = 160;  // K-blocks a CTA, for T tiles merged by slices
 constexpr int64_t kLocalTMaxWeightBytes = int64_t(80) << 20;
 constexpr int64_t kSwapMaxRows = 128;  // above this many token rows, tokens are the A operand
+constexpr bool kPairMma = true;       // large M: data-parallel tiles by CTA pairs (pair MMA)
 constexpr bool kSplitKAdapter = true;  // decode order: T by split K in the epilogue warps
 // (up to 64 token rows: the operands of a chunk are staged in the finisher
 // staging area, which exists for tiles of at most 64 tokens)
@@ -150,6 +152,7 @@ struct Params {
   int swap;
   int localt;  // swap path with per-piece adapter
   int tslice;  // (token-rows order) split T tiles merge and publish by slices
+  int pair;    // pair order: data-parallel tiles of 256 tokens by CTA pairs (pair_gemm_kernel)
   // Split-K adapter (decode order): the epilogue warps of CTA c < tchunks
   // compute the partial T of chunk c (tkpc K-blocks of one problem's d_in;
   // problem p owns chunks [tch0[p], tch0[p+1])), then reduce a slice of T.
@@ -1529,6 +1532,225 @@ grouped_lora_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constan
   }
 }
 
+// ------------------------------------------------------------- pair order
+// Large M with at least a wave of tiles: tiles of 256 tokens x bn outputs
+// (y: bn = 256; T: bn = the rank) in data-parallel waves, each computed by a
+// cluster of two CTAs with the pair MMA (M = 256).  CTA r of the pair loads
+// the tile's token rows [128 r, 128 r + 128) and its output rows
+// [r bn/2, (r + 1) bn/2) with plain TMA, every copy completing on the even
+// (leader) CTA's barrier; the leader's MMA thread multiplies both CTAs'
+// halves and its commits arrive on both CTAs' barriers; each CTA's TMEM
+// receives the accumulator rows of its own tokens, which its epilogue warps
+// store as in the token-rows order.  Per CTA and K-block 32 KB cross from L2
+// to shared memory instead of 48 KB for a 128 x 256 tile.  Tiles are dealt
+// t = pair, pair + pairs, ...; T tiles come first, so a y tile's adapter
+// K-blocks (the last of its K order) only wait for tiles that never wait.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairStage = 2 * kABytes;  // token half + output half (at most 128 rows)
+constexpr uint32_t kPairSmem = kPairStages * kPairStage + kBarrierBytes + kParamsBytes + 1024;
+constexpr uint32_t kPairTmemCols = 512;  // two 256-column accumulators
+
+__global__ void __launch_bounds__(kThreads, 1)
+pair_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params Pk) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStage);
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;  // [2] accumulator ready (both CTAs)
+  uint64_t* tempty = tfull + 2;           // [2] accumulator drained (leader: both CTAs' warps)
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  Params* sp = reinterpret_cast<Params*>(reinterpret_cast<uint8_t*>(full) + kBarrierBytes);
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&Pk);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(sp);
+    for (uint32_t i = threadIdx.x; i < sizeof(Params) / 4; i += kThreads) dst[i] = src[i];
+  }
+  const Params& P = *sp;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
+  static_assert((2 * kPairStages + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
+  static_assert(kPairSmem <= 227 * 1024 && kPairSmem > 114 * 1024, "one CTA per SM");
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 2 * (kEpiThreads / 32));
+    }
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, kPairTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
+
+  // Tile t of the data-parallel list: phase, token-tile pair and output tile.
+  auto tile_of = [&](int t, int& ph, int& ta2, int& tb) {
+    int p = P.dp0;
+    while (p + 1 < P.dp1 && P.ph[p + 1].tbase <= t) ++p;
+    ph = p;
+    tile_coords(P.ph[p], P.ph[p].tile0 + (t - P.ph[p].tbase), ta2, tb);
+  };
+
+  if (warp == 0 || warp == 6) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producers
+      const uint32_t mine = warp == 0 ? 0u : 1u;
+      const uint64_t pol = ptx::policy_evict_last();
+      uint32_t it = 0;
+      for (int t = pair; !*abort_flag && t < P.dp_tiles; t += npairs) {
+        int ph, ta2, tb;
+        tile_of(t, ph, ta2, tb);
+        const Phase& f = P.ph[ph];
+        const Prob& pb = P.pb[f.prob];
+        const CUtensorMap* mp = maps.m[f.prob];
+        const int nb = f.nkb - f.na;  // base K-blocks, then the adapter's
+        const uint32_t bytes = 2u * (kABytes + uint32_t(f.bn / 2) * kBK * 2u);
+        const int tok = ta2 * 2 * kBM + int(rank) * kBM;
+        const int outr = tb * f.bn + int(rank) * (f.bn / 2);
+        bool t_ok = false;
+        for (int i = 0; i < f.nkb; ++i, ++it) {
+          if ((it & 1u) != mine) continue;
+          const int s = int(it % kPairStages);
+          if (it >= uint32_t(kPairStages) &&
+              !ptx::mbar_wait(&empty[s], ((it / kPairStages) - 1) & 1, kWaitLimitNs)) {
+            *abort_flag = 1;
+            break;
+          }
+          const bool adapter = !f.down && i >= nb;
+          const int kc = (adapter ? i - nb : i) * kBK;
+          if (adapter && !t_ok) {
+            // both halves of the T tile of these 256 tokens are written
+            if (!wait_count(P.tflag + pb.tflag0 + ta2, 2, kWaitLimitNs)) *abort_flag = 1;
+            fence_proxy_async();
+            t_ok = true;
+          }
+          uint8_t* sa = smem + s * kPairStage;
+          const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[s]), 0);
+          if (leader) ptx::mbar_arrive_expect_tx(&full[s], bytes);
+          ptx::tma_load_2d_pair(sa, &mp[adapter ? MAP_T : MAP_X], bar, kc, tok, pol);
+          ptx::tma_load_2d_pair(sa + kABytes, &mp[f.down ? MAP_A : adapter ? MAP_B : MAP_W], bar, kc,
+                                f.down ? int(rank) * (f.bn / 2) : outr, pol);
+        }
+      }
+      // The leader's MMAs have read every stage this thread filled (their
+      // commits arrive here): no copy or arrival is left in flight at exit.
+      for (uint32_t j = it > uint32_t(kPairStages) ? it - kPairStages : 0; j < it; ++j)
+        if ((j & 1u) == mine) ptx::mbar_wait(&empty[j % kPairStages], (j / kPairStages) & 1, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t it = 0;
+      int seg = 0;
+      for (int t = pair; !*abort_flag && t < P.dp_tiles; t += npairs, ++seg) {
+        int ph, ta2, tb;
+        tile_of(t, ph, ta2, tb);
+        const Phase& f = P.ph[ph];
+        const int acc = seg & 1, use = seg >> 1;
+        if (seg >= 2 && !ptx::mbar_wait(&tempty[acc], (use - 1) & 1, kWaitLimitNs)) {
+          *abort_flag = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + uint32_t(acc * 256);
+        const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, f.bn);
+        bool ok = true;
+        for (int i = 0; i < f.nkb; ++i, ++it) {
+          const int s = int(it % kPairStages);
+          if (!ptx::mbar_wait(&full[s], (it / kPairStages) & 1, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + s * kPairStage);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int u = 0; u < kBK / kUmmaK; ++u)
+            ptx::umma_pair_f16(d, ptx::sw128_kmajor_desc(sa + u * 32), ptx::sw128_kmajor_desc(sb + u * 32),
+                               idesc, (i > 0 || u > 0) ? 1u : 0u);
+          ptx::umma_pair_commit(&empty[s], 3);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        ptx::umma_pair_commit(&tfull[acc], 3);
+      }
+      ptx::umma_pair_commit(mma_done, 1);
+      ptx::mbar_wait(mma_done, 0, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int et = threadIdx.x - 64;
+    int seg = 0;
+    for (int t = pair; t < P.dp_tiles; t += npairs, ++seg) {
+      int ph, ta2, tb;
+      tile_of(t, ph, ta2, tb);
+      const Phase& f = P.ph[ph];
+      const Prob& pb = P.pb[f.prob];
+      const int acc = seg & 1, use = seg >> 1;
+      const bool fail = !ptx::mbar_wait(&tfull[acc], use & 1, kWaitLimitNs);
+      if (epi_sync_or(fail || *abort_flag)) {
+        *abort_flag = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t tq = tmem + uint32_t(acc * 256) + (uint32_t(q * 32) << 16);
+      const int ta = ta2 * 2 + int(rank);  // this CTA's 128-token tile
+      for (int c0 = 0; c0 < f.bn; c0 += 16) {
+        float v[16];
+        tmem_ld16f(tq + c0, v);
+        store16(P, f, pb, ta, tb, row, c0, v, nullptr);
+      }
+      // the accumulator may be reused: one arrival per warp on the leader's barrier
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
+      if (f.down) {
+        // this CTA's half of the T tile, read next by TMA in other CTAs
+        fence_proxy_async();
+        epi_sync();
+        if (et == 0) {
+          fence_acq_rel_gpu();
+          red_add_relaxed(P.tflag + pb.tflag0 + ta2, 1);
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // neither CTA leaves while the other may still signal it
+  if (*abort_flag && threadIdx.x == 0) atomicOr(&g_device_error, 1);
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, kPairTmemCols);
+  }
+}
+
 // Clears the schedule's flags once the previous launch in the stream has
 // finished, letting the projection kernel that follows start right away.
 // (16-byte aligned, n16 16-byte words)
@@ -1591,7 +1813,12 @@ struct Layout {
 
 // Host-side schedule: the phases of both sections, the grid, each CTA's
 // ranges and the workspace layout.  Depends only on shapes and the SM count.
-bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms, Layout& L) {
+// Clusters of two CTAs that can be resident at once on this device for the
+// pair kernel (0 until the first launch has asked the runtime).
+std::atomic<int> g_pair_cap{0};
+
+bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms, Layout& L,
+                 bool allow_pair = true) {
   if (n < 1 || n > kMaxLoraProblems) return false;
   std::memset(&L, 0, sizeof(L));
   Params& P = L.P;
@@ -1622,6 +1849,85 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
   P.localt = (!P.tsplit && P.swap && any_rank && small_rank && wbytes < kLocalTMaxWeightBytes) ? 1 : 0;
   P.out_f32 = dtype == UNO_F32;
   const int bn_tok = pick_bn(M);
+
+  // Pair order (pair_gemm_kernel): token-rows M with at least a wave of
+  // 256-token tiles for the CTA pairs and every rank a multiple of 32 up to 256.
+  if (kPairMma && allow_pair && !P.swap && g_pair_cap.load() >= 0) {
+    const int cap = g_pair_cap.load();
+    const int pairs = std::max(1, std::min(std::min(sms, kMaxGrid) / 2, cap > 0 ? cap : kMaxGrid));
+    const int64_t ta2 = (M + 2 * kBM - 1) / (2 * kBM);
+    bool ranks_ok = true;
+    int64_t ptiles = 0;
+    for (int p = 0; p < n; ++p) {
+      ranks_ok = ranks_ok && pr[p].rank % 32 == 0 && pr[p].rank <= 256;
+      ptiles += (pr[p].rank > 0 ? ta2 : 0) + ta2 * ((pr[p].d_out + 255) / 256);
+    }
+    if (ranks_ok && ptiles >= pairs && ptiles < (int64_t(1) << 30) && 2 * n <= kMaxPhases) {
+      P.pair = 1;
+      P.grid = 2 * pairs;
+      P.bnmax = 256;
+      P.nprob = n;
+      int nph = 0, tflags = 0, tbase = 0;
+      for (int p = 0; p < n; ++p) {
+        Prob& b = P.pb[p];
+        b.d_in = int(pr[p].d_in);
+        b.d_out = int(pr[p].d_out);
+        b.r = int(pr[p].rank);
+        b.scale = pr[p].rank > 0 ? pr[p].alpha / float(pr[p].rank) : 0.f;
+        b.tflag0 = tflags;
+        if (pr[p].rank == 0) continue;
+        Phase f{};
+        f.prob = p;
+        f.down = 1;
+        f.nkb = int((pr[p].d_in + kBK - 1) / kBK);
+        f.tiles_a = int(ta2);
+        f.bn = int(pr[p].rank);
+        f.tiles = f.tiles_all = f.tiles_a;
+        f.tbase = tbase;
+        b.ttiles = f.tiles;
+        tflags += f.tiles;
+        tbase += f.tiles;
+        P.ph[nph++] = f;
+      }
+      for (int p = 0; p < n; ++p) {
+        Phase f{};
+        f.prob = p;
+        f.na = int((pr[p].rank + kBK - 1) / kBK);
+        f.nkb = f.na + int((pr[p].d_in + kBK - 1) / kBK);
+        f.tiles_a = int(ta2);
+        f.bn = 256;
+        f.tiles = f.tiles_all = int(ta2 * ((pr[p].d_out + 255) / 256));
+        f.tbase = tbase;
+        tbase += f.tiles;
+        P.ph[nph++] = f;
+      }
+      P.dp0 = 0;
+      P.dp1 = nph;
+      P.dp_tiles = tbase;
+      P.ph0[0] = P.ph1[0] = P.ph0[1] = P.ph1[1] = nph;
+      L.tflags = tflags;
+      size_t o = 0;
+      for (int p = 0; p < n; ++p) {
+        L.off_t[p] = o;
+        o = align_up(o + size_t(M) * size_t(pr[p].rank) * 2, 256);
+      }
+      L.off_tpart = L.off_partial = L.off_sync = o;
+      L.sync_bytes = align_up((2 * size_t(P.grid) + 2 * size_t(tflags)) * sizeof(int), 256);
+      o += L.sync_bytes;
+      if (dtype == UNO_F32) {
+        for (int p = 0; p < n; ++p) {
+          const size_t sz[4] = {size_t(M) * pr[p].d_in, size_t(pr[p].d_out) * pr[p].d_in,
+                                size_t(pr[p].rank) * pr[p].d_in, size_t(pr[p].d_out) * pr[p].rank};
+          for (int i = 0; i < 4; ++i) {
+            L.off_cast[p][i] = o;
+            o = align_up(o + sz[i] * 2, 256);
+          }
+        }
+      }
+      L.bytes = std::max<size_t>(o, 256);
+      return true;
+    }
+  }
 
   // Tile list: the T tiles of every adapted problem (unless each piece makes
   // its own), then the y tiles of every problem.
@@ -1919,13 +2225,70 @@ cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, grouped_lora_gemm_kernel<BNMAX, SWAP, LOCALT, STATS>, maps, P);
 }
 
+// The pair kernel's launch: clusters of two CTAs, chained like the others.
+cudaError_t pair_kernel_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(kPairSmem));
+  });
+  return err;
+}
+
+// Clusters of two that can be resident at once (asked once per process, on
+// the first launch; the schedule uses no more).
+void query_pair_cap() {
+  if (!kPairMma || g_pair_cap.load() != 0) return;
+  int n = 0;
+  if (pair_kernel_attr() == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(2 * std::max(1, sm_count() / 2)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  g_pair_cap.store(n > 0 ? n : -1);  // -1: no pair launches
+}
+
+cudaError_t launch_pair(const Maps& maps, const Params& P, cudaStream_t st) {
+  const cudaError_t a = pair_kernel_attr();
+  if (a != cudaSuccess) return a;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(P.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel, maps, P);
+}
+
 }  // namespace
 
 size_t lora_group_workspace_bytes(int n, const uno_lora_problem* pr, int64_t M, int dtype,
                                   int sms) {
-  Layout L;
-  if (!make_layout(n, pr, M, dtype, sms, L)) return 0;
-  return L.bytes;
+  // enough for the pair order and for the CTA-per-tile order (a launch with
+  // the statistics epilogue takes the latter)
+  auto Lp = std::make_unique<Layout>(), Lq = std::make_unique<Layout>();
+  if (!make_layout(n, pr, M, dtype, sms, *Lp)) return 0;
+  if (!make_layout(n, pr, M, dtype, sms, *Lq, false)) return 0;
+  return std::max(Lp->bytes, Lq->bytes);
 }
 
 // Host-side invariants of the schedule make_layout builds for `sms` CTAs
@@ -1946,7 +2309,7 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
   if (P.dp_tiles > 0) {
     int64_t t = 0;
     for (int p = P.dp0; p < P.dp1; ++p) t += P.ph[p].tiles;
-    if (P.swap || t != P.dp_tiles || P.dp_tiles < G) return 4;
+    if (P.swap || t != P.dp_tiles || P.dp_tiles < (P.pair ? G / 2 : G)) return 4;
   }
   int64_t sec_total[2] = {0, 0};
   for (int sec = 0; sec < 2; ++sec) {
@@ -2005,6 +2368,29 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
       if (P.lo[kDown][c] != P.lo[kDown][c + 1]) return 13;
     if ((2 * size_t(G) + 2 * size_t(L.tflags)) * sizeof(int) > L.sync_bytes) return 13;
   }
+  // 14: pair order: an even grid of at most one CTA per SM, data-parallel
+  // phases only (T tiles first, of the whole rank; y tiles 256 wide), tiles of
+  // 256 tokens, ranks that split into two TMA boxes, one T flag per T tile
+  if (P.pair) {
+    if (G % 2 || G < 2 || P.dp0 != 0 || P.ph0[0] != P.dp1 || sec_total[0] || sec_total[1] || P.swap ||
+        P.tsplit || P.localt || P.tslice)
+      return 14;
+    int flags = 0;
+    bool seen_y = false;
+    for (int p = P.dp0; p < P.dp1; ++p) {
+      const Phase& f = P.ph[p];
+      const Prob& b = P.pb[f.prob];
+      if (f.tiles_a != int((M + 2 * kBM - 1) / (2 * kBM)) || f.tiles != f.tiles_all) return 14;
+      if (f.down) {
+        if (seen_y || f.bn != b.r || b.r % 32 || b.r > 256 || f.na || b.tflag0 != flags) return 14;
+        flags += f.tiles;
+      } else {
+        seen_y = true;
+        if (f.bn != 256 || f.na != (b.r + kBK - 1) / kBK) return 14;
+      }
+    }
+    if (flags != L.tflags || (2 * size_t(G) + 2 * size_t(flags)) * sizeof(int) > L.sync_bytes) return 14;
+  }
   // 9: decode order only for decode-sized M
   if (P.swap != (M <= kSwapMaxRows ? 1 : 0)) return 9;
   // 10: workspace regions in order and inside the total
@@ -2054,7 +2440,7 @@ int logit_gemm_tiles(int64_t M, int64_t d, int64_t V, int sms) {
   p.d_in = d;
   p.d_out = V;
   Layout L;
-  if (!make_layout(1, &p, M, UNO_BF16, sms, L)) return 0;
+  if (!make_layout(1, &p, M, UNO_BF16, sms, L, false)) return 0;  // (the statistics epilogue's order)
   for (int i = 0; i < L.P.ph1[kMain]; ++i)
     if (!L.P.ph[i].down) return int((V + (L.P.swap ? kBM : L.P.ph[i].bn) - 1) / (L.P.swap ? kBM : L.P.ph[i].bn));
   return 0;
@@ -2086,7 +2472,7 @@ std::mutex g_plan_mu;
 
 int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w, size_t ws_bytes,
                int sms, const LinearEpilogue* epi, Layout& L, Maps& maps) {
-  if (!make_layout(n, pr, M, dtype, sms, L)) return UNO_ERR_ARG;
+  if (!make_layout(n, pr, M, dtype, sms, L, !(epi && epi->stats))) return UNO_ERR_ARG;
   if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
   Params& P = L.P;
   P.partial = reinterpret_cast<float*>(w + L.off_partial);
@@ -2125,6 +2511,11 @@ int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w,
       if (P.ph[i].prob == p) (P.ph[i].down ? bn_down : bn_main) = P.ph[i].bn;
     CUtensorMap* m = maps.m[p];
     const bool sw = P.swap != 0;
+    // pair order: each CTA loads half of a tile's output rows (bn / 2)
+    if (P.pair) {
+      bn_main /= 2;
+      bn_down /= 2;
+    }
     bool ok = encode_bf16(&m[MAP_X], x, q.d_in, M, sw ? bn_main : kBM) &&
               encode_bf16(&m[MAP_W], W, q.d_in, q.d_out, sw ? kBM : bn_main);
     if (ok && q.rank > 0) {
@@ -2177,6 +2568,7 @@ int launch_linear(int n, const uno_lora_problem* pr, int64_t M, int dtype, void*
     e.part = epi->part;
     e.gathered = epi->gathered;
   }
+  query_pair_cap();
   auto Lp = std::make_unique<Layout>();
   Layout& L = *Lp;
   Maps maps;
@@ -2240,7 +2632,9 @@ int launch_linear(int n, const uno_lora_problem* pr, int64_t M, int dtype, void*
     case 128: e = launch_grouped<128, SW, LT, ST>(maps, P, st); break;   \
     default: e = launch_grouped<256, SW, LT, ST>(maps, P, st); break;    \
   }
-  if (epi && epi->stats) {
+  if (P.pair) {
+    e = launch_pair(maps, P, st);
+  } else if (epi && epi->stats) {
     if (n != 1 || P.localt || pr[0].rank != 0) return UNO_ERR_UNSUPPORTED;
     if (P.swap) {
       UNO_DISPATCH(true, false, true)
