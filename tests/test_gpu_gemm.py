@@ -46,6 +46,13 @@ def _ref(pr, rows=None):
     (32, 16384, 64, 256, 512.0, torch.bfloat16, 16),   # split-K adapter chunks staged in several rounds
     (256, 14336, 1024, 128, 256.0, torch.bfloat16, 16),  # long T tiles, each in many pieces (token-rows order)
     (384, 1024, 512, 256, 512.0, torch.bfloat16, 16),    # rank 256 in token-rows order: 32 slices per T tile
+    # pair order (256-token tiles by CTA pairs, M > 128 with little padding and
+    # a tile for at least half of the pairs): ragged M and N, small ranks whose
+    # T tiles split into 16- and 32-row halves, rank 256, fp32 operands
+    (2660, 512, 1000, 64, 128.0, torch.bfloat16, 16),
+    (8192, 256, 256, 32, 64.0, torch.bfloat16, 16),
+    (4096, 768, 520, 256, 512.0, torch.bfloat16, 16),
+    (4096, 512, 512, 128, 256.0, torch.float32, 16),
 ])
 def test_lora_parity(M, d_in, d_out, r, alpha, dtype, block):
     pr = inputs.lora_problem(M, d_in, d_out, r, alpha, dtype=dtype, block=block,
