@@ -108,7 +108,11 @@ enum {
  * Residency: the kernel is persistent (one CTA per SM) and some CTAs wait,
  * with a 2-second limit, for partial sums that other CTAs of the same launch
  * publish (of output tiles and, for up to 64 rows, of the adapter input
- * x.A^T, which the CTAs compute by splitting d_in).  When other work keeps SMs from this launch (another
+ * x.A^T, which the CTAs compute by splitting d_in).  Large M (more than 128
+ * rows, with little padding of 256-row tiles) runs as clusters of two CTAs
+ * that share each 256-row tile through the pair MMA, no more clusters than
+ * the runtime reports resident; their output tiles wait, with the same limit,
+ * for the adapter-input tiles of the same launch.  When other work keeps SMs from this launch (another
  * stream's long kernel, an MPS or green-context SM limit) such a wait can run
  * out; the CTA then skips its output tile and sets bit 0 of the device error
  * word.  y is therefore defined only when uno_device_error() reads 0 after
@@ -164,7 +168,8 @@ typedef struct {
  * are partitioned over the CTAs in order, a split T tile's finisher takes no
  * other work (decode order) or a split T tile's pieces are whole CTA ranges
  * in consecutive CTAs (token-rows order), the adapter's d_in chunks cover every adapted problem with at
- * most one chunk per CTA, the workspace regions fit.  Returns 0 when all hold, a positive
+ * most one chunk per CTA, a pair-order launch has an even grid and 256-row
+ * tiles with the adapter-input tiles first, the workspace regions fit.  Returns 0 when all hold, a positive
  * invariant number otherwise, or UNO_ERR_ARG / UNO_ERR_UNSUPPORTED for
  * arguments the projection itself would refuse (pointers are not read). */
 int uno_lora_plan_check(int n, const uno_lora_problem *problems, int64_t M, int dtype, int sms);
