@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kThreads, kStatsCtasPerSm)
 verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
                     const int32_t* __restrict__ draft, int64_t K, int64_t Kp, int64_t V,
                     int splits, int64_t chunk, float inv_t, float2* __restrict__ part,
-                    float* __restrict__ gathered, int* __restrict__ counter) {
+                    float* __restrict__ gathered, int* __restrict__ counter,
+                    unsigned long long* __restrict__ keys, int key_stride) {
   const int64_t unit = blockIdx.x;
   const int64_t row = unit / splits;
   const int split = int(unit - row * splits);
@@ -74,7 +75,10 @@ verify_stats_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const int64_t b = row / per_seq;
   const int64_t j = row - b * per_seq;
   grid_dependency_wait();
-  if (j == 0 && split == 0 && threadIdx.x == 0) counter[b] = 0;  // finish kernel's arrival count
+  if (j == 0 && split == 0 && threadIdx.x == 0) {
+    counter[b] = 0;  // finish kernel's arrival count
+    if (keys) keys[b * key_stride] = keys[b * key_stride + 1] = 0ull;  // its race winners
+  }
   // This CTA's chunk [v0, v0 + n) of the row, addressed from its start with
   // 32-bit offsets (a chunk holds < 2^31 elements).
   const int64_t v0 = int64_t(split) * chunk;
@@ -153,8 +157,8 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
                      const float* __restrict__ u_res, int64_t K, int64_t Kp, int64_t V,
                      int splits, int race_splits, int64_t race_chunk, float inv_t, int mode,
                      const float2* __restrict__ part, const float* __restrict__ gathered,
-                     RacePart* __restrict__ rpart,
-                     int* __restrict__ counter, int32_t* __restrict__ n_acc,
+                     RacePart* __restrict__ rpart, unsigned long long* __restrict__ keys,
+                     int key_stride, int* __restrict__ counter, int32_t* __restrict__ n_acc,
                      int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_emit,
                      int32_t* __restrict__ status) {
   __shared__ float s_m[kMaxRows];    // row max
@@ -489,42 +493,23 @@ verify_finish_kernel(const float* __restrict__ p, const float* __restrict__ q,
     }
     int last = 1;
     if (race_splits > 1) {
-      rpart[b * race_splits + split] = RacePart{cr.s, cr.v, cp.s, cp.v};
+      // The chunk winners merge by atomic max of their keys; the count's
+      // release orders this CTA's maxima before it, and the last CTA's
+      // acquire orders every CTA's before its loads of the two keys.
+      unsigned long long* kk = keys + b * key_stride;
+      atomicMax(kk, cand_key(cr));
+      atomicMax(kk + 1, cand_key(cp));
       last = arrive_acq_rel(&counter[b]) == race_splits - 1;
+      if (last) {
+        cr = cand_of_key(__ldcg(kk));
+        cp = cand_of_key(__ldcg(kk + 1));
+        counter[b] = 0;
+      }
     }
     s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
-  if (race_splits > 1) {
-    // The last CTA of the sequence merges every chunk's winner (loads spread
-    // over the block, then the same warp/block reduction); thread 0's
-    // acquire and the barrier above order them after every chunk's store.
-    cr = Cand{0.f, -1};
-    cp = Cand{-1.f, -1};
-    for (int s = tid; s < race_splits; s += kThreads) {
-      const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
-      cr = cand_best(cr, Cand{__int_as_float(t.x), t.y});
-      cp = cand_best(cp, Cand{__int_as_float(t.z), t.w});
-    }
-    cr = warp_best(cr);
-    cp = warp_best(cp);
-    __syncthreads();
-    if ((tid & 31) == 0) {
-      s_cr[tid >> 5] = cr;
-      s_cp[tid >> 5] = cp;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      cr = s_cr[0];
-      cp = s_cp[0];
-      for (int w = 1; w < kWarps; ++w) {
-        cr = cand_best(cr, s_cr[w]);
-        cp = cand_best(cp, s_cp[w]);
-      }
-      counter[b] = 0;
-    }
-  }
   if (tid == 0) {
     n_acc[b] = n;
     n_emit[b] = n + 1;
@@ -635,10 +620,15 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(unsigned(g1));
+  // race winners' keys: the first 16 bytes of each sequence's race slots
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(rpart);
+  const int key_stride = 2 * std::max(pl.race_splits, pl.icdf_splits);
   cudaError_t e = ex ? cudaLaunchKernelEx(&cfg, verify_stats_kernel<true>, p, q, draft, K, Kp, V,
-                                          pl.splits, pl.chunk, inv_t, part, gathered, counter)
+                                          pl.splits, pl.chunk, inv_t, part, gathered, counter, keys,
+                                          key_stride)
                      : cudaLaunchKernelEx(&cfg, verify_stats_kernel<false>, p, q, draft, K, Kp, V,
-                                          pl.splits, pl.chunk, inv_t, part, gathered, counter);
+                                          pl.splits, pl.chunk, inv_t, part, gathered, counter, keys,
+                                          key_stride);
   if (e != cudaSuccess) return e;
   const bool icdf = mode == kInverseCdf;
   const int rs = icdf ? pl.icdf_splits : pl.race_splits;
@@ -646,12 +636,12 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
   cfg.gridDim = dim3(unsigned(Bn * rs));
   e = ex ? cudaLaunchKernelEx(&cfg, verify_finish_kernel<true>, p, q, draft, u_acc, u_res, K, Kp, V,
                               pl.splits, rs, rc, inv_t, mode,
-                              (const float2*)part, (const float*)gathered, rpart, counter, n_acc,
-                              out_tokens, n_emit, status)
+                              (const float2*)part, (const float*)gathered, rpart, keys, key_stride,
+                              counter, n_acc, out_tokens, n_emit, status)
          : cudaLaunchKernelEx(&cfg, verify_finish_kernel<false>, p, q, draft, u_acc, u_res, K, Kp,
                               V, pl.splits, pl.race_splits, pl.race_chunk, inv_t, mode,
-                              (const float2*)part, (const float*)gathered, rpart, counter, n_acc,
-                              out_tokens, n_emit, status);
+                              (const float2*)part, (const float*)gathered, rpart, keys, key_stride,
+                              counter, n_acc, out_tokens, n_emit, status);
   return e;
 }
 
@@ -671,7 +661,7 @@ cudaError_t launch_row_stats(const float* p, const float* q, const int32_t* draf
   return cudaLaunchKernelEx(&cfg, verify_stats_kernel<false>, p, q, draft, K, Kp, V, pl.splits,
                             pl.chunk, 1.0f, reinterpret_cast<float2*>(w + pl.off_stats),
                             reinterpret_cast<float*>(w + pl.off_gather),
-                            reinterpret_cast<int*>(w + pl.off_count));
+                            reinterpret_cast<int*>(w + pl.off_count), nullptr, 0);
 }
 
 cudaError_t launch_draft_sample(const float* logits, const float* u, int64_t R, int64_t V,

@@ -67,6 +67,22 @@ __device__ __forceinline__ Cand warp_best(Cand a) {
   return a;
 }
 
+// Candidates as 64-bit keys whose unsigned order is cand_best's: the score
+// (IEEE bits made order-preserving; NaN lowest) above the id (2^31 - v for
+// a token, 0 for none, so a lower id and a token over none win ties).  The
+// race's chunk winners then merge by atomic max, in any order.
+__device__ __forceinline__ unsigned long long cand_key(Cand c) {
+  uint32_t u = __float_as_uint(c.s);
+  u = isnan(c.s) ? 0u : (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t lo = c.v >= 0 ? 0x80000000u - uint32_t(c.v) : 0u;
+  return (static_cast<unsigned long long>(u) << 32) | lo;
+}
+__device__ __forceinline__ Cand cand_of_key(unsigned long long k) {
+  const uint32_t hi = uint32_t(k >> 32), lo = uint32_t(k);
+  const uint32_t u = (hi & 0x80000000u) ? (hi & 0x7FFFFFFFu) : ~hi;
+  return Cand{__uint_as_float(u), lo ? int(0x80000000u - lo) : -1};
+}
+
 struct RacePart {
   float sr;  // best residual score in the chunk (0 if no positive residual)
   int vr;
