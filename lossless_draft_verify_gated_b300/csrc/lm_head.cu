@@ -62,6 +62,7 @@ lm_decide_kernel(const __nv_bfloat16* __restrict__ h, const int32_t* __restrict_
                  int64_t d, int nvt, const float2* __restrict__ part,
                  const float* __restrict__ gathered, __nv_bfloat16* __restrict__ hc,
                  SeqDecision* __restrict__ dec, int* __restrict__ counter,
+                 unsigned long long* __restrict__ keys, int key_stride,
                  int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tokens,
                  int32_t* __restrict__ n_emit, int32_t* __restrict__ status) {
   __shared__ float s_m[kLMaxRows], s_lz[kLMaxRows], s_iz[kLMaxRows];
@@ -135,6 +136,7 @@ lm_decide_kernel(const __nv_bfloat16* __restrict__ h, const int32_t* __restrict_
     sd.izq = residual ? s_iz[Kp + n] : 0.f;
     dec[b] = sd;
     counter[b] = 0;
+    keys[b * key_stride] = keys[b * key_stride + 1] = 0ull;  // the race's winners
   }
   if (hc != nullptr) {
     // hidden states of the rows to race: hc[2b] = AR row prow, hc[2b+1] =
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kLT)
 lm_race_kernel(const float* __restrict__ logits, int recompute, const int32_t* __restrict__ draft,
                const float* __restrict__ u_res, int64_t Bn, int64_t K, int64_t Kp, int64_t V,
                int race_splits, int64_t race_chunk, const SeqDecision* __restrict__ dec,
-               RacePart* __restrict__ rpart, int* __restrict__ counter,
+               unsigned long long* __restrict__ keys, int key_stride, int* __restrict__ counter,
                int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tokens,
                int32_t* __restrict__ n_emit, int32_t* __restrict__ status) {
   __shared__ Cand s_cr[kLW], s_cp[kLW];
@@ -222,42 +224,23 @@ lm_race_kernel(const float* __restrict__ logits, int recompute, const int32_t* _
     }
     int last = 1;
     if (race_splits > 1) {
-      rpart[b * race_splits + split] = RacePart{cr.s, cr.v, cp.s, cp.v};
+      // chunk winners merge by atomic max of their keys (verify_common.cuh)
+      unsigned long long* kk = keys + b * key_stride;
+      atomicMax(kk, cand_key(cr));
+      atomicMax(kk + 1, cand_key(cp));
       __threadfence();
       last = atomicAdd(&counter[b], 1) == race_splits - 1;
+      if (last) {
+        __threadfence();
+        cr = cand_of_key(__ldcg(kk));
+        cp = cand_of_key(__ldcg(kk + 1));
+      }
     }
     s_last = last;
     s_tok = (residual && cr.v >= 0) ? cr.v : cp.v;
   }
   __syncthreads();
   if (!s_last) return;
-  if (race_splits > 1) {
-    __threadfence();
-    Cand br{0.f, -1}, bp{-1.f, -1};
-    for (int s = tid; s < race_splits; s += kLT) {
-      const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
-      br = cand_best(br, Cand{__int_as_float(t.x), t.y});
-      bp = cand_best(bp, Cand{__int_as_float(t.z), t.w});
-    }
-    br = warp_best(br);
-    bp = warp_best(bp);
-    __syncthreads();
-    if (lane == 0) {
-      s_cr[warp] = br;
-      s_cp[warp] = bp;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      br = s_cr[0];
-      bp = s_cp[0];
-      for (int w = 1; w < kLW; ++w) {
-        br = cand_best(br, s_cr[w]);
-        bp = cand_best(bp, s_cp[w]);
-      }
-      s_tok = (residual && br.v >= 0) ? br.v : bp.v;
-    }
-    __syncthreads();
-  }
   const int tok = s_tok;
   int32_t* out = out_tokens + b * (K + 1);
   for (int64_t i = tid; i <= K; i += kLT) out[i] = i < n ? draft[b * K + i] : (i == n ? tok : -1);
@@ -383,7 +366,8 @@ int launch_lm_head_verify(const void* h, const void* W, const int32_t* draft, co
                                      static_cast<const __nv_bfloat16*>(h), draft, u_acc, Bn, K, Kp,
                                      V, d, L.nvt, const_cast<const float2*>(epi.part),
                                      const_cast<const float*>(epi.gathered), hc, dec, counter,
-                                     n_acc, out_tokens, n_emit, status);
+                                     reinterpret_cast<unsigned long long*>(w + L.off_race),
+                                     2 * L.race_splits, n_acc, out_tokens, n_emit, status);
   if (e != cudaSuccess) return UNO_ERR_CUDA;
   const float* race_rows = logits;
   if (!store) {
@@ -401,8 +385,8 @@ int launch_lm_head_verify(const void* h, const void* W, const int32_t* draft, co
   cfg = pdl_config(dim3(unsigned(Bn * L.race_splits)), st, attr);
   e = cudaLaunchKernelEx(&cfg, lm_race_kernel, race_rows, store ? 0 : 1, draft, u_res, Bn, K, Kp, V,
                          L.race_splits, L.race_chunk, const_cast<const SeqDecision*>(dec),
-                         reinterpret_cast<RacePart*>(w + L.off_race), counter, n_acc, out_tokens,
-                         n_emit, status);
+                         reinterpret_cast<unsigned long long*>(w + L.off_race), 2 * L.race_splits,
+                         counter, n_acc, out_tokens, n_emit, status);
   return e == cudaSuccess ? UNO_OK : UNO_ERR_CUDA;
 }
 

@@ -44,7 +44,7 @@ tree_finish_kernel(const float* __restrict__ logits, const int32_t* __restrict__
                    const int32_t* __restrict__ token, const float* __restrict__ u_acc,
                    const float* __restrict__ u_res, int64_t N, int64_t V, int splits,
                    int race_splits, int64_t race_chunk, const float2* __restrict__ part,
-                   RacePart* __restrict__ rpart, int* __restrict__ counter,
+                   unsigned long long* __restrict__ keys, int key_stride, int* __restrict__ counter,
                    int32_t* __restrict__ n_acc, int32_t* __restrict__ path,
                    int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_emit,
                    int32_t* __restrict__ status) {
@@ -249,45 +249,24 @@ tree_finish_kernel(const float* __restrict__ logits, const int32_t* __restrict__
     }
     int last = 1;
     if (race_splits > 1) {
-      rpart[b * race_splits + split] = RacePart{cr.s, cr.v, cp.s, cp.v};
+      // chunk winners merge by atomic max of their keys (verify_common.cuh)
+      unsigned long long* kk = keys + b * key_stride;
+      atomicMax(kk, cand_key(cr));
+      atomicMax(kk + 1, cand_key(cp));
       __threadfence();
       last = atomicAdd(&counter[b], 1) == race_splits - 1;
+      if (last) {
+        __threadfence();
+        cr = cand_of_key(__ldcg(kk));
+        cp = cand_of_key(__ldcg(kk + 1));
+        counter[b] = 0;
+      }
     }
     s_last = last;
     s_tok_out = (cr.v >= 0) ? cr.v : cp.v;
   }
   __syncthreads();
   if (!s_last) return;
-  if (race_splits > 1) {
-    // merge every chunk's winners: loads spread over the block, then the warp
-    // and block reductions
-    __threadfence();
-    Cand br{0.f, -1}, bp{-1.f, -1};
-    for (int s = tid; s < race_splits; s += kTT) {
-      const int4 t = __ldcg(reinterpret_cast<const int4*>(rpart + b * race_splits + s));
-      br = cand_best(br, Cand{__int_as_float(t.x), t.y});
-      bp = cand_best(bp, Cand{__int_as_float(t.z), t.w});
-    }
-    br = warp_best(br);
-    bp = warp_best(bp);
-    __syncthreads();
-    if (lane == 0) {
-      s_cr[warp] = br;
-      s_cp[warp] = bp;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      br = s_cr[0];
-      bp = s_cp[0];
-      for (int w = 1; w < kTW; ++w) {
-        br = cand_best(br, s_cr[w]);
-        bp = cand_best(bp, s_cp[w]);
-      }
-      s_tok_out = br.v >= 0 ? br.v : bp.v;
-      counter[b] = 0;
-    }
-    __syncthreads();
-  }
   const int depth = s_depth;
   const int tok = s_tok_out;
   for (int64_t i = tid; i < N1; i += kTT)
@@ -308,7 +287,10 @@ cudaError_t launch_tree_verify(const float* logits, const int32_t* parent, const
                                int32_t* n_emit, int32_t* status, void* ws, const VerifyPlan& pl,
                                cudaStream_t st) {
   // node rows as the AR rows of a block with no draft rows (K = 0, Kp = N + 1)
-  cudaError_t e = launch_row_stats(logits, logits, parent, Bn, 0, N + 1, V, pl, ws, st);
+  // (the statistics pass also zeroes the race's arrival counts and winner keys)
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + pl.off_race);
+  const int key_stride = 2 * std::max(pl.race_splits, pl.icdf_splits);
+  cudaError_t e = launch_row_stats(logits, logits, parent, Bn, 0, N + 1, V, pl, ws, st, keys, key_stride);
   if (e != cudaSuccess) return e;
   char* w = static_cast<char*>(ws);
   cudaLaunchAttribute attr[1];
@@ -323,7 +305,7 @@ cudaError_t launch_tree_verify(const float* logits, const int32_t* parent, const
   return cudaLaunchKernelEx(&cfg, tree_finish_kernel, logits, parent, token, u_acc, u_res, N, V,
                             pl.splits, pl.race_splits, pl.race_chunk,
                             reinterpret_cast<const float2*>(w + pl.off_stats),
-                            reinterpret_cast<RacePart*>(w + pl.off_race),
+                            keys, key_stride,
                             reinterpret_cast<int*>(w + pl.off_count), n_acc, path, out_tokens,
                             n_emit, status);
 }

@@ -44,9 +44,11 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
 
 // The statistics pass alone over the rows of a plan (Bn sequences of Kp rows
 // of p then K rows of q); K = 0 gives plain per-row (max, sum exp) partials.
+// It zeroes each sequence's arrival count and, when `keys` is given, the two
+// race-winner keys at keys[b * key_stride] for the race that follows.
 cudaError_t launch_row_stats(const float* p, const float* q, const int32_t* draft, int64_t Bn,
                              int64_t K, int64_t Kp, int64_t V, const VerifyPlan& pl, void* ws,
-                             cudaStream_t st);
+                             cudaStream_t st, unsigned long long* keys = nullptr, int key_stride = 0);
 
 // ------------------------------------------------------------ tree sampler
 constexpr int64_t kTreeMaxNodes = 255;  // drafted nodes per sequence (N); N + 1 rows

@@ -647,7 +647,7 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
 
 cudaError_t launch_row_stats(const float* p, const float* q, const int32_t* draft, int64_t Bn,
                              int64_t K, int64_t Kp, int64_t V, const VerifyPlan& pl, void* ws,
-                             cudaStream_t st) {
+                             cudaStream_t st, unsigned long long* keys, int key_stride) {
   char* w = static_cast<char*>(ws);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -661,7 +661,7 @@ cudaError_t launch_row_stats(const float* p, const float* q, const int32_t* draf
   return cudaLaunchKernelEx(&cfg, verify_stats_kernel<false>, p, q, draft, K, Kp, V, pl.splits,
                             pl.chunk, 1.0f, reinterpret_cast<float2*>(w + pl.off_stats),
                             reinterpret_cast<float*>(w + pl.off_gather),
-                            reinterpret_cast<int*>(w + pl.off_count), nullptr, 0);
+                            reinterpret_cast<int*>(w + pl.off_count), keys, key_stride);
 }
 
 cudaError_t launch_draft_sample(const float* logits, const float* u, int64_t R, int64_t V,
