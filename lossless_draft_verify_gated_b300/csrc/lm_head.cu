@@ -154,8 +154,9 @@ lm_decide_kernel(const __nv_bfloat16* __restrict__ h, const int32_t* __restrict_
 }
 
 // One CTA per (sequence, vocabulary chunk): the exponential race over this
-// chunk of the residual row (or the bonus row), the last CTA to arrive
-// merges the chunk winners and writes the outputs (atomic count, no waiting).
+// chunk of the residual row (or the bonus row) and folds its winners into the
+// sequence's 64-bit keys by atomic max; the last CTA to arrive reads the keys
+// and writes the outputs (atomic count, no waiting).
 __global__ void __launch_bounds__(kLT)
 lm_race_kernel(const float* __restrict__ logits, int recompute, const int32_t* __restrict__ draft,
                const float* __restrict__ u_res, int64_t Bn, int64_t K, int64_t Kp, int64_t V,

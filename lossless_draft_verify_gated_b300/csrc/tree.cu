@@ -19,8 +19,9 @@
 //             merges its rows' partials, and warp 0 walks the tree (children
 //             found 32 at a time with a ballot, tested in index order); then
 //             each CTA races its chunk of the final node's row with the
-//             rejected tokens excluded, and the last CTA to arrive (atomic
-//             count, no waiting) merges the winners and writes the outputs.
+//             rejected tokens excluded (winners folded into 64-bit keys by
+//             atomic max), and the last CTA to arrive (atomic count, no
+//             waiting) reads the keys and writes the outputs.
 // Nothing spins, nothing traps: a malformed tree or a non-finite row on the
 // walked path sets the sequence's status.
 #include <algorithm>

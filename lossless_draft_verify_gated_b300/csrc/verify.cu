@@ -18,9 +18,10 @@
 //   finish -- one CTA per (sequence, vocab chunk); every CTA of a sequence
 //             merges the partials of that sequence (identically), takes the
 //             accept decisions and the prefix length n, then races its chunk
-//             of the residual row (or the bonus row); the last CTA to arrive
-//             (atomic counter, no waiting) merges the chunk winners and writes
-//             the outputs.
+//             of the residual row (or the bonus row), folds its winners into
+//             the sequence's two 64-bit keys by atomic max, and counts in; the
+//             last CTA to arrive (atomic counter, no waiting) reads the keys
+//             and writes the outputs.
 // Sampling variants (uno_verify_block_ex) are separate instantiations of both
 // kernels: logits scaled by 1/T, and optionally the single-uniform inverse CDF
 // in place of the race (exact fixed-point chunk sums; the last CTA finds the
