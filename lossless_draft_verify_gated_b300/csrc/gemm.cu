@@ -1550,6 +1550,9 @@ constexpr uint32_t kPairStage = 2 * kABytes;  // token half + output half (at mo
 constexpr uint32_t kPairSmem = kPairStages * kPairStage + kBarrierBytes + kParamsBytes + 1024;
 constexpr uint32_t kPairTmemCols = 512;  // two 256-column accumulators
 
+// STATS: the statistics epilogue of the verifier's logit rows (rank 0 only),
+// as in the CTA-per-tile order.
+template <bool STATS>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params Pk) {
   extern __shared__ uint8_t smem_raw[];
@@ -1720,10 +1723,27 @@ pair_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Para
       ptx::tc_fence_after();
       const uint32_t tq = tmem + uint32_t(acc * 256) + (uint32_t(q * 32) << 16);
       const int ta = ta2 * 2 + int(rank);  // this CTA's 128-token tile
-      for (int c0 = 0; c0 < f.bn; c0 += 16) {
-        float v[16];
-        tmem_ld16f(tq + c0, v);
-        store16(P, f, pb, ta, tb, row, c0, v, nullptr);
+      const int m_row = ta * kBM + row;
+      if constexpr (STATS) {
+        // (max, sum exp) of the row's columns in this vocabulary tile, and the
+        // logit of the row's drafted token where the tile holds it
+        const int xd_row = m_row < P.M ? row_draft_token(pb, m_row) : -1;
+        float dummy_gather;
+        vfy::MS sacc{-INFINITY, 0.f};
+        for (int c0 = 0; c0 < f.bn; c0 += 16) {
+          float v[16];
+          tmem_ld16f(tq + c0, v);
+          if (pb.st_store) store16(P, f, pb, ta, tb, row, c0, v, nullptr);
+          stats16_rows(f, pb, tb, c0, v, xd_row, m_row < P.M,
+                       m_row < P.M ? pb.st_gather + m_row : &dummy_gather, sacc);
+        }
+        if (m_row < P.M) pb.st_part[int64_t(m_row) * pb.st_nvt + tb] = make_float2(sacc.m, sacc.s);
+      } else {
+        for (int c0 = 0; c0 < f.bn; c0 += 16) {
+          float v[16];
+          tmem_ld16f(tq + c0, v);
+          store16(P, f, pb, ta, tb, row, c0, v, nullptr);
+        }
       }
       // the accumulator may be reused: one arrival per warp on the leader's barrier
       ptx::tc_fence_before();
@@ -2232,11 +2252,12 @@ cudaError_t launch_grouped(const Maps& maps, const Params& P, cudaStream_t st) {
 }
 
 // The pair kernel's launch: clusters of two CTAs, chained like the others.
+template <bool STATS>
 cudaError_t pair_kernel_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(pair_gemm_kernel<STATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                int(kPairSmem));
   });
   return err;
@@ -2247,7 +2268,7 @@ cudaError_t pair_kernel_attr() {
 void query_pair_cap() {
   if (!kPairMma || g_pair_cap.load() != 0) return;
   int n = 0;
-  if (pair_kernel_attr() == cudaSuccess) {
+  if (pair_kernel_attr<false>() == cudaSuccess) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(2 * std::max(1, sm_count() / 2)));
     cfg.blockDim = dim3(kThreads);
@@ -2259,14 +2280,15 @@ void query_pair_cap() {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<false>, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
   g_pair_cap.store(n > 0 ? n : -1);  // -1: no pair launches
 }
 
+template <bool STATS>
 cudaError_t launch_pair(const Maps& maps, const Params& P, cudaStream_t st) {
-  const cudaError_t a = pair_kernel_attr();
+  const cudaError_t a = pair_kernel_attr<STATS>();
   if (a != cudaSuccess) return a;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(P.grid));
@@ -2282,7 +2304,7 @@ cudaError_t launch_pair(const Maps& maps, const Params& P, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel, maps, P);
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<STATS>, maps, P);
 }
 
 }  // namespace
@@ -2441,15 +2463,27 @@ int launch_logit_gemm(const uno_lora_problem& pr, int64_t M, void* ws, size_t ws
   return launch_linear(1, &pr, M, UNO_BF16, ws, ws_bytes, st, &epi);
 }
 
+namespace {
+// Vocabulary tiles per logit row in a layout (the statistics epilogue leaves
+// one (max, sum exp) per row and tile).
+int layout_vocab_tiles(const Layout& L, int64_t V) {
+  for (int i = 0; i < L.P.ph1[kMain]; ++i)
+    if (!L.P.ph[i].down) {
+      const int w = L.P.swap ? kBM : L.P.ph[i].bn;
+      return int((V + w - 1) / w);
+    }
+  return 0;
+}
+}  // namespace
+
 int logit_gemm_tiles(int64_t M, int64_t d, int64_t V, int sms) {
   uno_lora_problem p{};
   p.d_in = d;
   p.d_out = V;
-  Layout L;
-  if (!make_layout(1, &p, M, UNO_BF16, sms, L, false)) return 0;  // (the statistics epilogue's order)
-  for (int i = 0; i < L.P.ph1[kMain]; ++i)
-    if (!L.P.ph[i].down) return int((V + (L.P.swap ? kBM : L.P.ph[i].bn) - 1) / (L.P.swap ? kBM : L.P.ph[i].bn));
-  return 0;
+  query_pair_cap();  // the same schedule as the launch
+  auto L = std::make_unique<Layout>();
+  if (!make_layout(1, &p, M, UNO_BF16, sms, *L)) return 0;
+  return layout_vocab_tiles(*L, V);
 }
 
 namespace {
@@ -2478,7 +2512,7 @@ std::mutex g_plan_mu;
 
 int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w, size_t ws_bytes,
                int sms, const LinearEpilogue* epi, Layout& L, Maps& maps) {
-  if (!make_layout(n, pr, M, dtype, sms, L, !(epi && epi->stats))) return UNO_ERR_ARG;
+  if (!make_layout(n, pr, M, dtype, sms, L)) return UNO_ERR_ARG;
   if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
   Params& P = L.P;
   P.partial = reinterpret_cast<float*>(w + L.off_partial);
@@ -2638,8 +2672,16 @@ int launch_linear(int n, const uno_lora_problem* pr, int64_t M, int dtype, void*
     case 128: e = launch_grouped<128, SW, LT, ST>(maps, P, st); break;   \
     default: e = launch_grouped<256, SW, LT, ST>(maps, P, st); break;    \
   }
+  // the statistics partials are laid out by the vocabulary tiles the caller
+  // planned for: a launch whose tiles differ would write past them
+  if (epi && epi->stats && layout_vocab_tiles(L, pr[0].d_out) != epi->nvt) return UNO_ERR_ARG;
   if (P.pair) {
-    e = launch_pair(maps, P, st);
+    if (epi && epi->stats) {
+      if (n != 1 || pr[0].rank != 0) return UNO_ERR_UNSUPPORTED;
+      e = launch_pair<true>(maps, P, st);
+    } else {
+      e = launch_pair<false>(maps, P, st);
+    }
   } else if (epi && epi->stats) {
     if (n != 1 || P.localt || pr[0].rank != 0) return UNO_ERR_UNSUPPORTED;
     if (P.swap) {
