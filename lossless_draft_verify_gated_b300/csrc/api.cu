@@ -1,6 +1,9 @@
 // api.cu -- the extern "C" boundary of libuno.so (declared in include/uno.h):
 // argument validation, workspace queries and dispatch to the kernels.
 // Everything here runs on the host and touches no device memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 #include <mutex>
 
@@ -10,6 +13,38 @@ namespace uno {
 
 int read_device_error(int reset);  // gemm.cu
 
+namespace {
+// SMs of the current context's SM resource when the driver reports one (a
+// green context may own fewer SMs than the device); 0 when it does not.
+int context_sm_count() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetDevResource_v12040 get_res = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetDevResource", &p, 12040, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_res = reinterpret_cast<PFN_cuCtxGetDevResource_v12040>(p);
+    cudaGetLastError();
+  });
+  if (!get_cur || !get_res) return 0;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  CUdevResource r{};
+  if (get_res(ctx, &r, CU_DEV_RESOURCE_TYPE_SM) != CUDA_SUCCESS) return 0;
+  return int(r.sm.smCount);
+}
+}  // namespace
+
+// SMs the persistent kernels may size their grids for: the device's, or the
+// current context's SM resource where that is smaller.  (An MPS client's
+// thread-percentage limit is not visible here; the kernels' bounded waits
+// and the device error word cover that case.)
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -25,7 +60,8 @@ int sm_count() {
     }
     cached[dev] = n;
   }
-  return cached[dev];
+  const int c = context_sm_count();
+  return c > 0 && c < cached[dev] ? c : cached[dev];
 }
 
 namespace {

@@ -66,6 +66,7 @@
 #include <cstring>
 #include <memory>
 #include <atomic>
+#include <vector>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -97,7 +98,9 @@ constexpr bool kSplitKAdapter = true;  // decode order: T by split K in the epil
 constexpr int64_t kSplitKMaxRows = 64;
 constexpr int kDown = 0, kMain = 1;
 
-enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, kMapsPerProblem = 5 };
+// MAP_W2 / MAP_B2: (pair order) W and B with 64-row boxes, for the 128-wide
+// tiles that finish a launch's last wave
+enum { MAP_X = 0, MAP_W = 1, MAP_A = 2, MAP_B = 3, MAP_T = 4, MAP_W2 = 5, MAP_B2 = 6, kMapsPerProblem = 7 };
 
 struct Maps {
   CUtensorMap m[kMaxLoraProblems][kMapsPerProblem];
@@ -117,6 +120,7 @@ struct Phase {
   int prob;
   int down;          // 1: T = gate*scale*x.A^T;  0: y = T.B^T + x.W^T
   int bn;            // MMA N (B-operand rows per tile)
+  int n0;            // (pair order) first output column of the phase's tiles
 };
 
 struct Prob {
@@ -489,7 +493,7 @@ __device__ __forceinline__ void store16(const Params& P, const Phase& f, const P
     // lane = token m, accumulator column = output column n
     const int m = ta * kBM + row;
     if (m >= P.M) return;
-    const int n0 = tb * f.bn + c0;
+    const int n0 = f.n0 + tb * f.bn + c0;
     const float gs = f.down ? float(pb.gate[m]) * pb.scale : 1.f;
     if (!f.down && (P.out_f32 || pb.f32out)) {
       float* d = static_cast<float*>(pb.y) + int64_t(m) * ncols;
@@ -1628,7 +1632,8 @@ pair_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Para
         const int nb = f.nkb - f.na;  // base K-blocks, then the adapter's
         const uint32_t bytes = 2u * (kABytes + uint32_t(f.bn / 2) * kBK * 2u);
         const int tok = ta2 * 2 * kBM + int(rank) * kBM;
-        const int outr = tb * f.bn + int(rank) * (f.bn / 2);
+        const int outr = f.n0 + tb * f.bn + int(rank) * (f.bn / 2);
+        const bool narrow = !f.down && f.bn == 128;  // 64-row boxes
         bool t_ok = false;
         for (int i = 0; i < f.nkb; ++i, ++it) {
           if ((it & 1u) != mine) continue;
@@ -1650,8 +1655,9 @@ pair_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Para
           const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&full[s]), 0);
           if (leader) ptx::mbar_arrive_expect_tx(&full[s], bytes);
           ptx::tma_load_2d_pair(sa, &mp[adapter ? MAP_T : MAP_X], bar, kc, tok, pol);
-          ptx::tma_load_2d_pair(sa + kABytes, &mp[f.down ? MAP_A : adapter ? MAP_B : MAP_W], bar, kc,
-                                f.down ? int(rank) * (f.bn / 2) : outr, pol);
+          ptx::tma_load_2d_pair(sa + kABytes,
+                                &mp[f.down ? MAP_A : adapter ? (narrow ? MAP_B2 : MAP_B) : (narrow ? MAP_W2 : MAP_W)],
+                                bar, kc, f.down ? int(rank) * (f.bn / 2) : outr, pol);
         }
       }
       // The leader's MMAs have read every stage this thread filled (their
@@ -1838,7 +1844,7 @@ struct Layout {
 std::atomic<int> g_pair_cap{0};
 
 bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sms, Layout& L,
-                 bool allow_pair = true) {
+                 bool allow_pair = true, bool no_narrow = false) {
   if (n < 1 || n > kMaxLoraProblems) return false;
   std::memset(&L, 0, sizeof(L));
   Params& P = L.P;
@@ -1888,7 +1894,7 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
     }
     const bool pad_ok = (ta2 * 2 * kBM - M) * 10 <= M;
     if (pairs >= 1 && ranks_ok && pad_ok && 2 * ptiles >= pairs && ptiles < (int64_t(1) << 30) &&
-        2 * n <= kMaxPhases) {
+        3 * n <= kMaxPhases) {
       P.pair = 1;
       P.grid = 2 * pairs;
       P.bnmax = 256;
@@ -1915,14 +1921,79 @@ bool make_layout(int n, const uno_lora_problem* pr, int64_t M, int dtype, int sm
         tbase += f.tiles;
         P.ph[nph++] = f;
       }
+      // y tiles 256 wide, except that when the last wave would keep at most
+      // half of the pairs busy, trailing 256-column groups (of the last
+      // problems first) become 128-wide tiles, dealt after all others, so
+      // that they fill the last wave: the count is the one whose simulated
+      // makespan (tiles dealt t -> pair t mod pairs; a 128-wide tile costs
+      // 3/4 of a 256-wide one per K-block) is least.  Not for the statistics
+      // epilogue, whose per-row partials assume one tile width.
+      int cols[kMaxLoraProblems];
+      int64_t total_cols = 0;
+      for (int p = 0; p < n; ++p) total_cols += cols[p] = int((pr[p].d_out + 255) / 256);
+      auto split_of = [&](int64_t c, int (&conv)[kMaxLoraProblems]) {
+        for (int p = n - 1; p >= 0; --p) {
+          conv[p] = int(std::min<int64_t>(c, cols[p]));
+          c -= conv[p];
+        }
+      };
+      auto makespan = [&](int64_t c) {
+        int conv[kMaxLoraProblems];
+        split_of(c, conv);
+        std::vector<double> load(size_t(pairs), 0.0);
+        int64_t t = 0;
+        auto deal = [&](int64_t count, double cost) {
+          for (int64_t i = 0; i < count; ++i, ++t) load[size_t(t % pairs)] += cost;
+        };
+        for (int p = 0; p < n; ++p)
+          if (pr[p].rank > 0) deal(ta2, double((pr[p].d_in + kBK - 1) / kBK) * 0.75);
+        for (int p = 0; p < n; ++p)
+          deal(ta2 * (cols[p] - conv[p]), double((pr[p].rank + kBK - 1) / kBK + (pr[p].d_in + kBK - 1) / kBK));
+        for (int p = 0; p < n; ++p)
+          if (conv[p] > 0) {
+            const int64_t n0 = int64_t(cols[p] - conv[p]) * 256;
+            deal(ta2 * ((pr[p].d_out - n0 + 127) / 128),
+                 0.75 * double((pr[p].rank + kBK - 1) / kBK + (pr[p].d_in + kBK - 1) / kBK));
+          }
+        return *std::max_element(load.begin(), load.end());
+      };
+      int64_t best_c = 0;
+      if (!no_narrow && (ptiles % pairs) * 2 <= pairs && ptiles % pairs != 0) {
+        double best = makespan(0);
+        const int64_t cmax = std::min<int64_t>(total_cols, (pairs + ta2 - 1) / ta2 + 1);
+        for (int64_t c = 1; c <= cmax; ++c) {
+          const double m = makespan(c);
+          if (m < best * 0.999) {
+            best = m;
+            best_c = c;
+          }
+        }
+      }
+      int conv[kMaxLoraProblems];
+      split_of(best_c, conv);
       for (int p = 0; p < n; ++p) {
+        if (cols[p] - conv[p] == 0) continue;
         Phase f{};
         f.prob = p;
         f.na = int((pr[p].rank + kBK - 1) / kBK);
         f.nkb = f.na + int((pr[p].d_in + kBK - 1) / kBK);
         f.tiles_a = int(ta2);
         f.bn = 256;
-        f.tiles = f.tiles_all = int(ta2 * ((pr[p].d_out + 255) / 256));
+        f.tiles = f.tiles_all = int(ta2 * (cols[p] - conv[p]));
+        f.tbase = tbase;
+        tbase += f.tiles;
+        P.ph[nph++] = f;
+      }
+      for (int p = 0; p < n; ++p) {
+        if (conv[p] == 0) continue;
+        Phase f{};
+        f.prob = p;
+        f.na = int((pr[p].rank + kBK - 1) / kBK);
+        f.nkb = f.na + int((pr[p].d_in + kBK - 1) / kBK);
+        f.tiles_a = int(ta2);
+        f.bn = 128;
+        f.n0 = (cols[p] - conv[p]) * 256;
+        f.tiles = f.tiles_all = int(ta2 * ((pr[p].d_out - f.n0 + 127) / 128));
         f.tbase = tbase;
         tbase += f.tiles;
         P.ph[nph++] = f;
@@ -2414,8 +2485,21 @@ int lora_plan_check(int n, const uno_lora_problem* pr, int64_t M, int dtype, int
         flags += f.tiles;
       } else {
         seen_y = true;
-        if (f.bn != 256 || f.na != (b.r + kBK - 1) / kBK) return 14;
+        if ((f.bn != 256 && f.bn != 128) || f.na != (b.r + kBK - 1) / kBK || f.n0 % 256 ||
+            f.tiles_all % f.tiles_a)
+          return 14;
       }
+    }
+    // every problem's output columns are covered once, in ascending phases
+    for (int q = 0; q < n; ++q) {
+      int64_t next = 0;
+      for (int p = P.dp0; p < P.dp1; ++p) {
+        const Phase& f = P.ph[p];
+        if (f.down || f.prob != q) continue;
+        if (f.n0 != next) return 14;
+        next = f.n0 + int64_t(f.tiles_all / f.tiles_a) * f.bn;
+      }
+      if (next < pr[q].d_out || next - pr[q].d_out >= 256) return 14;
     }
     if (flags != L.tflags || (2 * size_t(G) + 2 * size_t(flags)) * sizeof(int) > L.sync_bytes) return 14;
   }
@@ -2482,7 +2566,7 @@ int logit_gemm_tiles(int64_t M, int64_t d, int64_t V, int sms) {
   p.d_out = V;
   query_pair_cap();  // the same schedule as the launch
   auto L = std::make_unique<Layout>();
-  if (!make_layout(1, &p, M, UNO_BF16, sms, *L)) return 0;
+  if (!make_layout(1, &p, M, UNO_BF16, sms, *L, true, true)) return 0;  // (the statistics epilogue's)
   return layout_vocab_tiles(*L, V);
 }
 
@@ -2512,7 +2596,7 @@ std::mutex g_plan_mu;
 
 int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w, size_t ws_bytes,
                int sms, const LinearEpilogue* epi, Layout& L, Maps& maps) {
-  if (!make_layout(n, pr, M, dtype, sms, L)) return UNO_ERR_ARG;
+  if (!make_layout(n, pr, M, dtype, sms, L, true, epi && epi->stats)) return UNO_ERR_ARG;
   if (ws_bytes < L.bytes) return UNO_ERR_WORKSPACE;
   Params& P = L.P;
   P.partial = reinterpret_cast<float*>(w + L.off_partial);
@@ -2546,9 +2630,12 @@ int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w,
       b.st_part = epi->part;
       b.st_gather = epi->gathered;
     }
-    int bn_main = 0, bn_down = 0;
+    int bn_main = 0, bn_down = 0;  // the widest tiles of the problem (pair order: also 128-wide ones)
     for (int i = 0; i < P.ph1[kMain]; ++i)
-      if (P.ph[i].prob == p) (P.ph[i].down ? bn_down : bn_main) = P.ph[i].bn;
+      if (P.ph[i].prob == p) {
+        int& w = P.ph[i].down ? bn_down : bn_main;
+        w = std::max(w, P.ph[i].bn);
+      }
     CUtensorMap* m = maps.m[p];
     const bool sw = P.swap != 0;
     // pair order: each CTA loads half of a tile's output rows (bn / 2)
@@ -2564,6 +2651,14 @@ int build_plan(int n, const uno_lora_problem* pr, int64_t M, int dtype, char* w,
            encode_bf16(&m[MAP_T], b.t, q.rank, M, sw ? bn_main : kBM);
     } else {
       m[MAP_A] = m[MAP_B] = m[MAP_T] = m[MAP_X];
+    }
+    // (pair order) 64-row boxes of W and B for the 128-wide tiles
+    if (ok && P.pair) {
+      ok = encode_bf16(&m[MAP_W2], W, q.d_in, q.d_out, 64) &&
+           (q.rank == 0 || encode_bf16(&m[MAP_B2], B, q.rank, q.d_out, 64));
+      if (q.rank == 0) m[MAP_B2] = m[MAP_W2];
+    } else {
+      m[MAP_W2] = m[MAP_B2] = m[MAP_X];
     }
     if (!ok) return UNO_ERR_CUDA;
   }
