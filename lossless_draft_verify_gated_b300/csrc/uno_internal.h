@@ -25,6 +25,7 @@ bool verify_shape_ok(int64_t Bn, int64_t K, int64_t Kp, int64_t V);
 
 struct VerifyPlan {
   int64_t rows;      // Bn * (Kp + K): AR rows then draft rows of each sequence
+  int stats_cps;     // statistics CTAs per SM (the kernel's occupancy and load depth)
   int splits;        // vocab chunks per row in the statistics pass
   int64_t chunk;     // elements per chunk (multiple of 4)
   int race_splits;   // vocab chunks per sequence in the resampling race
