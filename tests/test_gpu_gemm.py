@@ -109,8 +109,9 @@ def test_operand_order_boundaries(M):
 
 
 def test_large_m_deterministic_and_gate_zero_rows():
-    """Data-parallel waves at M = 2048: two calls give the same bits, and
-    gate-0 rows equal a call with every gate 0."""
+    """Data-parallel waves at M = 2048 (the pair order, 256-token tiles by CTA
+    pairs): two calls give the same bits, and gate-0 rows equal a call with
+    every gate 0."""
     pr = inputs.lora_problem(2048, 4096, 4096, 128, 256.0, block=16, name="det.large")
     a, b = _gpu_run(pr), _gpu_run(pr)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
@@ -189,6 +190,23 @@ def test_batched_mixed_ranks_and_shapes(M):
     ys = _batched(prs)
     for pr, y in zip(prs, ys):
         assert gemm_err(y, _ref(pr)) <= GEMM_TOL
+
+
+def test_batched_pair_order_mixed_ranks():
+    """The pair order with ranks 0, 32, 64 and 128 in one launch (T tiles whose
+    halves are 16, 32 and 64 output rows), ragged d_in and d_out, and a last
+    problem whose trailing columns run as a 128-wide tile (8 real columns):
+    64 seeded rows against the oracle over every column."""
+    M = 2048
+    shapes = [(512, 1000, 32, 64.0), (256, 520, 0, 1.0), (1024, 2048, 128, 256.0), (384, 264, 64, 128.0)]
+    prs = [inputs.lora_problem(M, di, do, r, a, block=16, name=f"pairmix.{i}")
+           for i, (di, do, r, a) in enumerate(shapes)]
+    ys = _batched(prs)
+    rows = torch.randperm(M, generator=inputs.generator("rows.pairmix"))[:64]
+    for pr, y in zip(prs, ys):
+        assert gemm_err(y[rows.cuda()], _ref(pr, rows)) <= GEMM_TOL
+    from lossless_draft_verify_gated_b300 import uno_device_error
+    assert uno_device_error() == 0
 
 
 def test_batched_fp32():
