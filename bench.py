@@ -345,9 +345,11 @@ class Step:
 
 
 class Timer:
-    """Replays the two halves of a step (projections, verifier) from CUDA graphs
-    and times each half with CUDA events on the launching stream, with an L2
-    flush (a write of twice the L2 size) before every step outside the events."""
+    """Replays a step from CUDA graphs and times it with CUDA events on the
+    launching stream, with an L2 flush before every step outside the events.
+    The step is one graph (projections then verifier, chained as a serving
+    loop would launch them); each half is also timed alone, from a graph of its
+    own, for the projections' roofline and the verifier's fields."""
 
     def __init__(self, st, dev, graph=True, l2_flush="write_read"):
         import torch
@@ -356,6 +358,7 @@ class Timer:
         self.flush_read = (torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
                            if l2_flush == "write_read" else None)
         self.g_proj = self.g_ver = None
+        self.g_step = []
         if graph:
             s = torch.cuda.Stream(device=dev)
             s.wait_stream(torch.cuda.current_stream())
@@ -374,6 +377,14 @@ class Timer:
                 with torch.cuda.graph(g):
                     st.verify(k)
                 self.g_ver.append(g)
+            self.g_step = []
+            if st.groups:
+                for k in range(len(st.vsets)):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        st.projections()
+                        st.verify(k)
+                    self.g_step.append(g)
 
     def proj(self):
         if self.g_proj is not None:
@@ -398,29 +409,54 @@ class Timer:
             self.flush()
             self.proj()
             self.ver(i)
+            if self.g_step:
+                self.flush()
+                self.g_step[self.st.set_of_step(i)].replay()
         torch.cuda.synchronize()
 
     def run(self, steps, barrier=None):
-        """Per-step (step, projections, verifier) milliseconds and the wall time."""
+        """Per-step (step, projections, verifier) milliseconds and the wall
+        time of the step's timed region.  With graphs, the step times come from
+        the one-graph steps (the timed region the wall time covers); the two
+        halves are then timed alone over as many steps again."""
         import torch
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        whole = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
         if barrier:
             barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(steps):
-            self.flush()  # L2 flush, outside the timed events
-            ev[i][0].record()
-            self.proj()
-            ev[i][1].record()
-            self.ver(i)
-            ev[i][2].record()
+        if self.g_step:
+            for i in range(steps):
+                self.flush()  # L2 flush, outside the timed events
+                whole[i][0].record()
+                self.g_step[self.st.set_of_step(i)].replay()
+                whole[i][1].record()
+        else:
+            for i in range(steps):
+                self.flush()
+                ev[i][0].record()
+                self.proj()
+                ev[i][1].record()
+                self.ver(i)
+                ev[i][2].record()
         torch.cuda.synchronize()
         if barrier:
             barrier()
         wall = time.perf_counter() - t0
-        return ([e[0].elapsed_time(e[2]) for e in ev], [e[0].elapsed_time(e[1]) for e in ev],
-                [e[1].elapsed_time(e[2]) for e in ev], wall)
+        if self.g_step:
+            for i in range(steps):
+                self.flush()
+                ev[i][0].record()
+                self.proj()
+                ev[i][1].record()
+                self.ver(i)
+                ev[i][2].record()
+            torch.cuda.synchronize()
+            t_step = [w[0].elapsed_time(w[1]) for w in whole]
+        else:
+            t_step = [e[0].elapsed_time(e[2]) for e in ev]
+        return (t_step, [e[0].elapsed_time(e[1]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev], wall)
 
 
 def proj_roofline(M, n_gate1, ms_proj, hbm, tflops):
@@ -665,7 +701,9 @@ def run_uno(args):
         "config": config_dict(args, args.batch, ws),
         "verified_tokens_per_step": round(tokens, 3),
         "verifier_input_sets": len(st.vsets),
-        "launch": "CUDA graph per half-step" if tm.g_ver is not None else "eager",
+        "launch": ("one CUDA graph per step; projections and verifier also timed alone, a graph each, "
+                   "for their fields" if tm.g_step else
+                   "CUDA graph per half-step" if tm.g_ver is not None else "eager"),
         "inputs": "CPU-drawn seeded inputs copied to the device" if check_parity else
                   "seeded inputs drawn on the device",
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,

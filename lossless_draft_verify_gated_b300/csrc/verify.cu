@@ -614,11 +614,15 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
   RacePart* rpart = reinterpret_cast<RacePart*>(w + pl.off_race);
   int* counter = reinterpret_cast<int*>(w + pl.off_count);
   const int64_t g1 = pl.rows * pl.splits;
-  // Both kernels are launched with programmatic stream serialization: each
-  // may start while the launch before it drains, and waits for it
-  // (griddepcontrol.wait) before it reads anything that launch writes.  The
-  // statistics CTAs signal the finish kernel only as they end, so its CTAs
-  // become resident as the statistics wave drains, not during it.
+  // The finish kernel is launched with programmatic stream serialization: it
+  // may start while the statistics pass drains, and waits for it
+  // (griddepcontrol.wait) before it reads what that pass writes; the
+  // statistics CTAs signal it only as they end, so its CTAs become resident
+  // as the statistics wave drains, not during it.  The statistics kernel
+  // itself is launched in plain stream order: placed early beside a
+  // still-running projection launch, its CTAs found fewer free slots per SM
+  // than the plan's single wave assumes (a batch-32 step in one graph took
+  // 0.498 ms that way against 0.475 ms).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -628,6 +632,7 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(unsigned(g1));
+  cfg.numAttrs = 0;  // (statistics: plain stream order)
   // race winners' keys: the first 16 bytes of each sequence's race slots
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(rpart);
   const int key_stride = 2 * std::max(pl.race_splits, pl.icdf_splits);
@@ -637,6 +642,7 @@ cudaError_t launch_verify(const float* p, const float* q, const int32_t* draft,
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p, q, draft, K, Kp, V, pl.splits, pl.chunk, inv_t, part,
                                      gathered, counter, keys, key_stride);
   if (e != cudaSuccess) return e;
+  cfg.numAttrs = 1;  // (finish: chained to the statistics pass)
   const bool icdf = mode == kInverseCdf;
   const int rs = icdf ? pl.icdf_splits : pl.race_splits;
   const int64_t rc = icdf ? pl.icdf_chunk : pl.race_chunk;
@@ -663,7 +669,7 @@ cudaError_t launch_row_stats(const float* p, const float* q, const int32_t* draf
   cfg.blockDim = dim3(kThreads);
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 0;  // plain stream order, as in launch_verify
   cfg.gridDim = dim3(unsigned(pl.rows * pl.splits));
   auto kern = pl.stats_cps == kStatsCtasPerSmFew ? verify_stats_kernel<false, kStatsCtasPerSmFew>
                                                  : verify_stats_kernel<false, kStatsCtasPerSm>;
