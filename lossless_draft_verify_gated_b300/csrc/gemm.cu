@@ -48,7 +48,12 @@
 // of T over the chunks in a fixed order and publishes it; the weight stream
 // never carries the down matrix and no T tile waits on a merge.  Larger
 // M takes tiles of 128 tokens x 256 (or 128) outputs and, with at least one
-// tile per CTA, deals whole tiles out in data-parallel waves (no splits).
+// tile per CTA, deals whole tiles out in data-parallel waves (no splits); a
+// split T tile of that order is merged by slices over its pieces when a
+// CTA's share of K-blocks is short.  With 256-token tiles for at least half
+// of the CTA pairs and little padding, a launch runs instead as clusters of
+// two CTAs (pair_gemm_kernel, below): 256 x 256 tiles by the pair MMA, each
+// CTA loading half of every operand.
 // Launches are chained with programmatic dependent launch: each CTA lets the
 // next launch in the stream start at once, and waits (griddepcontrol.wait)
 // for the previous one before it touches global memory, except for L2
