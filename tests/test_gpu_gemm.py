@@ -229,12 +229,15 @@ def test_batched_deterministic():
 LAYER_GROUPS = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]
 
 
-@pytest.mark.parametrize("M", [256, 1024, 4096, 16384])
+@pytest.mark.parametrize("M", [256, 512, 1024, 4096, 16384])
 def test_layer_groups_sweep_sampled(M):
     """The layer's projections as the benchmark launches them (one grouped
     launch each for q/k/v, o, gate/up and down) at the row counts of the batch
-    sweep (batch 8, 32, 128, 512 x 2 x block 16): 64 seeded rows, half gate 0
-    and half gate 1, against the oracle over every column."""
+    sweep (batch 8, 32, 128, 512 x 2 x block 16) and at batch 16 (q/k/v and
+    gate/up in the pair order, gate/up with a 128-wide tail; o and down in
+    token-rows stream-K):
+    64 seeded rows, half gate 0 and half gate 1, against the oracle over every
+    column."""
     layer = dict(inputs.llama3_layer(M, rank=128, alpha=256.0, block=16))
     g = inputs.generator(f"rows.sweep.{M}")
     perm = torch.randperm(M, generator=g)
