@@ -233,6 +233,12 @@ SWEEP_LM_BATCHES = (1, 256)
 SWEEP_TREE = ((1, (3, 2, 2, 1)), (8, (3, 2, 2, 1)))  # (batch, children per node at each depth)
 
 
+def n_verify_sets(batch):
+    """Verifier input sets that consecutive steps cycle through (step i verifies
+    set i mod n, in every arm and in the end-to-end figure)."""
+    return max(1, VERIFY_SET_SEQS // batch)
+
+
 def config_dict(args, batch, ws):
     """The workload, identical in both arms (run details sit outside it)."""
     return {"workload": workload_name(batch), "batch": batch, "block": BLOCK, "vocab": VOCAB,
@@ -284,11 +290,12 @@ class Step:
         self.plain = temperature == 1.0 and resample == "race"
         # Verifier inputs: at a small batch the accepted lengths of a single draw
         # say little about the mean, so consecutive steps cycle through several
-        # seeded input sets (at least VERIFY_SET_SEQS sequences in all).  Set 0
-        # is the one drawn as host_inputs asks (the one the oracle sample reads).
+        # seeded input sets (at least VERIFY_SET_SEQS sequences in all), every
+        # one drawn as host_inputs asks (with the CPU generators, the oracle's
+        # arms draw the same sets).
         self.vsets = []
-        for k in range(max(1, VERIFY_SET_SEQS // batch)):
-            vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=gen_dev if k == 0 else device,
+        for k in range(n_verify_sets(batch)):
+            vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, device=gen_dev,
                                        seed=inputs.BASE_SEED + k)
             if vp.p_logits.device != torch.device(device):
                 vp = inputs.VerifyProblem(*(t.to(device) for t in (vp.p_logits, vp.q_logits, vp.u_accept,
@@ -727,7 +734,10 @@ def run_uno(args):
         out["roofline"]["frac_of_sustained"] = round(achieved / tflops_sustained, 4)
     out["clocks"] = clk.summary()
     if not args.no_e2e:
-        out["e2e"] = e2e(st, dev, max(5, min(K, 50)), ws)
+        # whole rounds of the verifier input sets, so that its tokens per step
+        # are the same mean as the device-timed figure's over many rounds
+        nv = len(st.vsets)
+        out["e2e"] = e2e(st, dev, nv * max(1, -(-max(5, min(K, 50)) // nv)), ws)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         if st.plain:
             out["cpu_baseline"] = cpu_baseline(st, args.batch, args.sigma, budget_s=15.0,
@@ -749,44 +759,46 @@ def run_uno(args):
 def e2e(st, dev, steps, ws=1):
     """Same metric through the public API with host buffers: every step copies
     its inputs host->device from pinned memory, runs the ops eagerly and reads
-    the verified tokens back.  Also reported: the time of the copies alone and
-    the host time spent in the API calls (enqueue, no synchronisation)."""
+    the verified tokens back.  Step i verifies input set i mod n, as the
+    device-timed steps do.  Also reported: the time of the copies alone and the
+    host time spent in the API calls (enqueue, no synchronisation)."""
     import torch
-    host = {}
+    layer_host = []
     seen = set()
-    for i, (_, p) in enumerate(st.layer):
-        for tag, t in (("x", p.x), ("g", p.gate)):
+    for _, p in st.layer:
+        for t in (p.x, p.gate):
             if t.data_ptr() not in seen:  # q/k/v and gate/up share their input; one gate tensor
                 seen.add(t.data_ptr())
-                host[f"{tag}{i}"] = (t.cpu().pin_memory(), t)
-    for k in ("p", "q", "draft", "ua", "ur"):
-        t = getattr(st, k)
-        host[k] = (t.cpu().pin_memory(), t)
-    h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
-    outs = [torch.empty_like(st.vout[1], device="cpu").pin_memory(),
-            torch.empty_like(st.vout[2], device="cpu").pin_memory()]
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+                layer_host.append((t.cpu().pin_memory(), t))
+    n = min(steps, len(st.vsets))
+    set_host = [[(st.vsets[k][f].cpu().pin_memory(), st.vsets[k][f]) for f in ("p", "q", "draft", "ua", "ur")]
+                for k in range(n)]
+    h2d = sum(h.numel() * h.element_size() for h, _ in layer_host + set_host[0])
+    outs = [[torch.empty_like(st.vsets[k]["vout"][i], device="cpu").pin_memory() for i in (1, 2)]
+            for k in range(n)]
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
     torch.cuda.synchronize()
 
-    def copies():
-        for h, d in host.values():
+    def copies(k):
+        for h, d in layer_host + set_host[k]:
             d.copy_(h, non_blocking=True)
 
-    def one():
-        copies()
+    def one(i):
+        k = i % n
+        copies(k)
         st.projections()
-        st.verify()
-        outs[0].copy_(st.vout[1], non_blocking=True)
-        outs[1].copy_(st.vout[2], non_blocking=True)
+        st.verify(k)
+        outs[k][0].copy_(st.vsets[k]["vout"][1], non_blocking=True)
+        outs[k][1].copy_(st.vsets[k]["vout"][2], non_blocking=True)
 
-    for _ in range(3):
-        one()
+    for i in range(3):
+        one(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # the copies alone
     e0.record()
-    for _ in range(steps):
-        copies()
+    for i in range(steps):
+        copies(i % n)
     e1.record()
     torch.cuda.synchronize()
     ms_copy = e0.elapsed_time(e1) / steps
@@ -802,28 +814,37 @@ def e2e(st, dev, steps, ws=1):
     if ws > 1:
         torch.distributed.barrier()
     e0.record()
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(i)
     e1.record()
     torch.cuda.synchronize()
     check_device_error()
-    ms, tokens = aggregate(e0.elapsed_time(e1) / steps, int(outs[1].sum()), ws, dev)
+    # every set's outputs are the same at each of its steps (seeded inputs)
+    per_step = sum(int(outs[i % n][1].sum()) for i in range(steps)) / steps
+    ms, tokens = aggregate(e0.elapsed_time(e1) / steps, per_step, ws, dev)
     return {"value": round(tokens / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_ms_per_step": round(ms_copy, 4), "host_api_ms_per_step": round(t_api / steps * 1e3, 4),
             "launch": "eager API calls"}
 
 
-def cpu_inputs(batch, sigma):
-    """The same workload drawn on the host (CPU generators), drafts drawn by
-    the oracle's own sampler."""
+def cpu_verify_set(batch, sigma, k):
+    """Verifier input set k drawn on the host (CPU generators, as the GPU arm
+    draws it for the headline), drafts drawn by the oracle's own sampler."""
     from lossless_draft_verify_gated_b300 import inputs
     import oracle
+    vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma, seed=inputs.BASE_SEED + k)
+    draft, _, margin = oracle.draft_sample(vp.q_logits, vp.u_draft)
+    return vp, draft.reshape(batch, BLOCK), margin.reshape(batch, BLOCK)
+
+
+def cpu_inputs(batch, sigma):
+    """The same workload drawn on the host (CPU generators): the layer and
+    verifier input set 0."""
+    from lossless_draft_verify_gated_b300 import inputs
     M = 2 * BLOCK * batch
     layer = inputs.llama3_layer(M, rank=RANK, alpha=ALPHA, block=BLOCK)
-    vp = inputs.verify_problem(batch, BLOCK, VOCAB, sigma=sigma)
-    draft, _, margin = oracle.draft_sample(vp.q_logits, vp.u_draft)
-    return layer, vp, draft.reshape(batch, BLOCK), margin.reshape(batch, BLOCK)
+    return (layer,) + cpu_verify_set(batch, sigma, 0)
 
 
 class OracleStep:
@@ -835,9 +856,11 @@ class OracleStep:
     def __init__(self, batch, sigma):
         import oracle
         oracle.build()
-        self.batch = batch
+        self.batch, self.sigma = batch, sigma
         self.M = 2 * BLOCK * batch
         self.layer, self.vp, self.draft, self.draft_margin = cpu_inputs(batch, sigma)
+        self.nsets = n_verify_sets(batch)
+        self.vsets = {0: (self.vp, self.draft, self.draft_margin)}
         self.threads = oracle.num_threads()
         self.rows = min(self.M, max(2, self.threads))
         self.seqs = min(batch, max(1, self.threads))
@@ -850,8 +873,30 @@ class OracleStep:
         M, rows = self.M, self.rows
         return np.concatenate([np.arange(rows // 2), M - 1 - np.arange(rows - rows // 2)])
 
-    def run(self):
+    def vset(self, k):
+        """Verifier input set k (drawn on first use, outside any timing)."""
+        if k not in self.vsets:
+            self.vsets[k] = cpu_verify_set(self.batch, self.sigma, k)
+        return self.vsets[k]
+
+    def verify_sample(self, k):
+        """The oracle's verifier on the sampled sequences of set k."""
         import oracle
+        vp, draft, _ = self.vset(k)
+        s = self.seqs
+        return oracle.verify_block(vp.p_logits[:s], vp.q_logits[:s], draft[:s], vp.u_accept[:s],
+                                   vp.u_resample[:s])
+
+    def mean_tokens(self):
+        """Verified tokens per step averaged over the sets that consecutive steps
+        cycle through (the sampled sequences of each, scaled to the batch)."""
+        return sum(float(self.verify_sample(k).n_emitted.sum()) for k in range(self.nsets)) \
+            * (self.batch / self.seqs) / self.nsets
+
+    def run(self, k=0):
+        """One timed sample of the step, its verifier on input set k."""
+        import oracle
+        self.vset(k)
         M, rows = self.M, self.rows
         r_idx = self.row_index()
         tp = tv = 0.0
@@ -869,13 +914,11 @@ class OracleStep:
                 scale_p = (M / rows) * (d_out / c)  # equal fractions for every projection
             t1 = time.perf_counter()
             s = self.seqs
-            vp = self.vp
-            r = oracle.verify_block(vp.p_logits[:s], vp.q_logits[:s], self.draft[:s], vp.u_accept[:s],
-                                    vp.u_resample[:s])
+            r = self.verify_sample(k)
             t2 = time.perf_counter()
             tp += t1 - t0
             tv += t2 - t1
-        self.last = (r_idx, ys, r)
+        self.last = (r_idx, ys, r) if k == 0 else None
         t_full = (tp * scale_p + tv * (self.batch / s)) / self.repeat
         tokens = float(r.n_emitted.sum()) * (self.batch / s)
         return t_full, tokens, tp + tv
@@ -929,9 +972,14 @@ class OracleStep:
 def cpu_baseline(st, batch, sigma, budget_s=15.0, compare=False):
     ob = OracleStep(batch, sigma)
     ob.calibrate(budget_s)
-    t_full, tokens, t_cpu = ob.run()
+    t_full, _, t_cpu = ob.run()
+    # tokens per step: the mean over the verifier input sets that the GPU arm's
+    # steps cycle through (the oracle's verifier on each set's sampled sequences)
+    tokens = ob.mean_tokens()
     out = {"value": round(tokens / t_full, 4), "unit": UNIT, "cores": ob.threads, "kind": "oracle",
-           "sample": ob.describe(1) + f"; {t_cpu:.1f} s of CPU work",
+           "sample": ob.describe(1) + f"; {t_cpu:.1f} s of CPU work; verified tokens per step: the "
+                     f"oracle's mean over the {ob.nsets} verifier input set(s) of the step",
+           "verified_tokens_per_step": round(tokens, 3),
            "ms_per_step_extrapolated": round(t_full * 1e3, 2)}
     if compare:
         out["parity"] = ob.compare(st)
@@ -950,7 +998,9 @@ def run_reference(args):
     ob.calibrate(min(1.0, 120.0 / max(1, args.steps + args.warmup)))
     times, toks = [], []
     for i in range(args.warmup + args.steps):
-        t_full, tokens, _ = ob.run()
+        # timed step j verifies input set j mod n, as the GPU arm's step j does
+        j = i - args.warmup if i >= args.warmup else i
+        t_full, tokens, _ = ob.run(j % ob.nsets)
         if i >= args.warmup:
             times.append(t_full)
             toks.append(tokens)
@@ -963,7 +1013,8 @@ def run_reference(args):
         "data": "synthetic",
         "config": config_dict(args, args.batch, ws),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": ob.threads, "kind": "oracle",
-                         "sample": ob.describe(args.steps)},
+                         "sample": ob.describe(args.steps) +
+                                   f"; timed step j verifies input set j mod {ob.nsets}"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }), flush=True)

@@ -30,3 +30,26 @@ def test_reference_arm_json_line():
     import bench
     assert d["config"]["workload"] == bench.workload_name(1)
     assert d["metric"] == bench.METRIC
+
+
+def test_oracle_arms_draw_the_gpu_arms_verifier_sets():
+    """The oracle's arms verify the input sets that the GPU arm's headline
+    steps cycle through (set k drawn with the CPU generators from seed
+    BASE_SEED + k, set 0 the one of the parity sample), and count tokens per
+    step as the mean over those sets."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    from lossless_draft_verify_gated_b300 import inputs
+    ob = bench.OracleStep(1, 1.0)
+    assert ob.nsets == bench.n_verify_sets(1) == bench.VERIFY_SET_SEQS
+    assert bench.n_verify_sets(8) == 8 and bench.n_verify_sets(512) == 1
+    assert ob.vset(0)[0] is ob.vp
+    vp3, draft3, _ = ob.vset(3)
+    ref = inputs.verify_problem(1, bench.BLOCK, bench.VOCAB, sigma=1.0, seed=inputs.BASE_SEED + 3)
+    assert torch.equal(vp3.p_logits, ref.p_logits) and torch.equal(vp3.u_resample, ref.u_resample)
+    assert not torch.equal(vp3.p_logits, ob.vp.p_logits)
+    assert draft3.shape == (1, bench.BLOCK)
+    ob.nsets = 3  # the mean over the first three sets, verified one by one
+    want = sum(float(ob.verify_sample(k).n_emitted.sum()) for k in range(3)) / 3
+    assert ob.mean_tokens() == want
