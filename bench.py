@@ -734,11 +734,7 @@ def run_uno(args):
         out["roofline"]["frac_of_sustained"] = round(achieved / tflops_sustained, 4)
     out["clocks"] = clk.summary()
     if not args.no_e2e:
-        # the verifier input sets of the device-timed steps: all K of them when
-        # they are at most one round of the sets, else whole rounds (the mean
-        # that many rounds approach)
-        nv = len(st.vsets)
-        out["e2e"] = e2e(st, dev, K if K <= nv else nv * max(1, min(K, 50) // nv), ws)
+        out["e2e"] = e2e(st, dev, e2e_steps(K, len(st.vsets)), ws)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         if st.plain:
             out["cpu_baseline"] = cpu_baseline(st, args.batch, args.sigma, budget_s=15.0,
@@ -755,6 +751,14 @@ def run_uno(args):
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def e2e_steps(K, n_sets):
+    """Steps of the end-to-end figure: the verifier input sets of the K
+    device-timed steps, all K of them when they are at most one round of the
+    n sets, else whole rounds (the mean that many rounds approach), about 50
+    steps where a round is shorter."""
+    return K if K <= n_sets else n_sets * max(1, min(K, 50) // n_sets)
 
 
 def e2e(st, dev, steps, ws=1):

@@ -53,3 +53,16 @@ def test_oracle_arms_draw_the_gpu_arms_verifier_sets():
     ob.nsets = 3  # the mean over the first three sets, verified one by one
     want = sum(float(ob.verify_sample(k).n_emitted.sum()) for k in range(3)) / 3
     assert ob.mean_tokens() == want
+
+
+def test_end_to_end_steps_cover_the_timed_steps_sets():
+    """The end-to-end figure verifies the sets of the K device-timed steps: all
+    K of them up to one round of the sets, else whole rounds."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.e2e_steps(20, 64) == 20
+    assert bench.e2e_steps(64, 64) == 64
+    assert bench.e2e_steps(2000, 64) == 64
+    assert bench.e2e_steps(2000, 8) == 48
+    assert bench.e2e_steps(2000, 1) == 50
+    assert bench.e2e_steps(3, 1) == 3

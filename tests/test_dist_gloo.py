@@ -23,8 +23,10 @@ def _worker(rank, ws, port, q):
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     import bench
     ms, tokens = bench.aggregate([1.25, 3.5][rank], [17, 40][rank], ws, "cpu")
+    # (the end-to-end figure passes a mean number of tokens per step)
+    _, frac = bench.aggregate(1.0, [2.5, 0.25][rank], ws, "cpu")
     dist.barrier()
-    q.put((rank, ms, tokens))
+    q.put((rank, ms, tokens, frac))
     dist.destroy_process_group()
 
 
@@ -39,7 +41,7 @@ def test_aggregate_over_two_gloo_ranks():
         p.join(timeout=120)
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
-    assert got == [(0, 3.5, 57), (1, 3.5, 57)]
+    assert got == [(0, 3.5, 57, 2.75), (1, 3.5, 57, 2.75)]
 
 
 def test_single_rank_is_untouched():
